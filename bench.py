@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark of the EXL3 trellis linear on one GB300 (or N replicas).
+
+Workload (decode rows at the 27B shapes): K = 5120, 4-bit trellis codes, 16
+rows of FP16 activations. One step is one q/k/v group call (N = 6144 + 1024 +
+1024: one rotation launch and one linear launch) followed by one single call on
+a 5120 x 5120 weight: the whole hot path (rotation, weight stream, decode, MMA,
+split-K combine with self-resetting counters, output rotation) over one batch.
+
+Metric: weight-stream GB/s (packed code bytes of every weight the step reads /
+step time), with µs per call alongside. Weights cycle through enough distinct
+copies that every step streams from HBM (> 4x the 129 MB L2). The CPU oracle
+is timed on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+K = 5120
+BITS = 4
+ROWS = 16
+QKV = (6144, 1024, 1024)
+O_N = 5120
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "EXL3 linear weight-stream GB/s (µs/call alongside) vs HBM roofline, decode rows at 27B shapes"
+
+
+def packed_bytes(Kk, N, bits):
+    return Kk * N * bits // 8
+
+
+STEP_WEIGHT_BYTES = sum(packed_bytes(K, n, BITS) for n in QKV) + packed_bytes(K, O_N, BITS)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        loaded = [v for v in sm if smax and v > 0.3 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, ws: int, device) -> float:
+    """Max of a float over ranks (the slowest rank's time decides)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(seconds_budget: float = 15.0):
+    """Time the CPU oracle on a bounded sample: the 5120 x 5120 layer at 16 rows,
+    columns [0, 512) (four 128-column blocks), repeated while the budget lasts."""
+    import numpy as np
+
+    import oracle
+    import synth
+    n = 512
+    codes = synth.codes(0, K, O_N, BITS)
+    suh = synth.suh(0, K).astype(np.float64)
+    svh = synth.svh(0, O_N).astype(np.float64)
+    x = synth.as_f64(synth.activations(0, ROWS, K, "f16"), "f16")
+    oracle.lib()
+    times = []
+    t_end = time.perf_counter() + seconds_budget
+    while True:
+        t0 = time.perf_counter()
+        oracle.linear(codes, K, n, BITS, suh, svh[:n], x, tile_row_stride=(O_N // 16) * 8 * BITS)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end or len(times) >= 50:
+            break
+    sec = statistics.median(times)
+    gbs = packed_bytes(K, n, BITS) / sec / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"5120x{n} columns of the 5120x5120 4-bit layer, {ROWS} rows, FP64 single-thread C; "
+                      f"median of {len(times)} calls ({sec * 1e3:.1f} ms/call)"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    import synth
+    n = 512
+    codes = synth.codes(0, K, O_N, BITS)
+    suh = synth.suh(0, K).astype(np.float64)
+    svh = synth.svh(0, O_N).astype(np.float64)
+    x = synth.as_f64(synth.activations(0, ROWS, K, "f16"), "f16")
+    oracle.lib()
+
+    def step():
+        oracle.linear(codes, K, n, BITS, suh, svh[:n], x, tile_row_stride=(O_N // 16) * 8 * BITS)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = (time.perf_counter() - t0) / args.steps
+    gbs = packed_bytes(K, n, BITS) / sec / 1e9
+    sample = (f"5120x{n} columns of the 5120x5120 4-bit layer, {ROWS} rows, per step; FP64 single-thread C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode rows at 27B shapes (sampled columns)", "K": K, "N": O_N, "bits": BITS,
+                       "rows": ROWS},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU leg
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import exl3_trellis_quantized_rot_gb300 as tfx
+    import synth
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+
+    # weights: enough distinct copies of the step's four weights to exceed 4x L2
+    copies = max(2, -(-4 * L2_BYTES // STEP_WEIGHT_BYTES))
+
+    def up(seed, N, member):
+        codes = synth.codes(seed, K, N, BITS, member)
+        t = torch.from_numpy(codes.view(np.int32)).to(dev)
+        su = torch.from_numpy(synth.suh(seed, K, member).view(np.int16)).to(dev)
+        sv = torch.from_numpy(synth.svh(seed, N, member).view(np.int16)).to(dev)
+        w = tfx.Weight(t, su, sv, K, N, BITS, tfx.F16)
+        tfx.reserve(w, ROWS, stream)
+        return w
+
+    base = [up(1000 + rank, N, m) for m, N in enumerate(QKV)] + [up(1000 + rank, O_N, 3)]
+    sets = []
+    for c in range(copies):
+        ws_c = []
+        for w in base:
+            t = w._keep[0].clone()  # same codes, distinct memory
+            wc = tfx.Weight(t, w._keep[1], w._keep[2], K, w.N, BITS, tfx.F16)
+            tfx.reserve(wc, ROWS, stream)
+            ws_c.append(wc)
+        sets.append(ws_c)
+    x = torch.from_numpy(synth.activations(1000 + rank, ROWS, K, "f16")).to(dev)
+    ys = [torch.empty((ROWS, n), dtype=torch.float16, device=dev) for n in QKV]
+    yo = torch.empty((ROWS, O_N), dtype=torch.float16, device=dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+
+    def step(i, marks=None):
+        q, k, v, o = sets[i % copies]
+        if marks:
+            tfx.mark_events(*marks[0])
+        tfx.group([q, k, v], x, ROWS, ys, stream)
+        if marks:
+            tfx.mark_events(*marks[1])
+        tfx.linear(o, x, ROWS, yo, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # device-resident timing, with the linear kernels' own events on the launching stream
+    kern_pairs = []
+    with ClockSampler(local) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+            step(i, pairs)
+            kern_pairs.append(pairs)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    clocks = clk.summary()
+    ms = start.elapsed_time(stop)
+    ms_max = reduce_max(ms, ws, dev)
+    sec_per_step = ms_max / 1e3 / args.steps
+    value = ws * STEP_WEIGHT_BYTES / sec_per_step / 1e9
+
+    # dominant kernel: the linear kernel (group launch and single launch)
+    kern_ms = [[a.elapsed_time(b) for (a, b) in p] for p in kern_pairs]
+    grp_ms = statistics.mean(k[0] for k in kern_ms)
+    one_ms = statistics.mean(k[1] for k in kern_ms)
+
+    def alg_bytes(Ns):
+        # packed codes + rotated x read + svh + y written (split-K scratch excluded)
+        return sum(packed_bytes(K, n, BITS) + 2 * ROWS * K + 2 * n + 2 * ROWS * n for n in Ns)
+
+    achieved = (alg_bytes(QKV) + alg_bytes([O_N])) / ((grp_ms + one_ms) / 1e3) / 1e9
+    peak, peak_kind = load_peaks()
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "linear_kernel_traffic.json")
+    if os.path.exists(tp):
+        d = json.load(open(tp))
+        if d.get("kernel_source_sha256") == kernel_source_hash():
+            traffic = d.get("bytes_per_launch_decode_rows_step")
+
+    # end-to-end: pinned host x -> device, the two calls, y -> pinned host, every step
+    xh = x.cpu().pin_memory()
+    yh = [torch.empty((ROWS, n), dtype=torch.float16).pin_memory() for n in QKV + (O_N,)]
+    xd = torch.empty_like(x)
+    for i in range(3):
+        xd.copy_(xh, non_blocking=True)
+        step(i)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        xd.copy_(xh, non_blocking=True)
+        q, k, v, o = sets[i % copies]
+        tfx.group([q, k, v], xd, ROWS, ys, stream)
+        tfx.linear(o, xd, ROWS, yo, stream)
+        for hbuf, dbuf in zip(yh, ys + [yo]):
+            hbuf.copy_(dbuf, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), ws, dev)
+    e2e_value = ws * STEP_WEIGHT_BYTES / (e2e_ms / 1e3 / args.steps) / 1e9
+
+    # per-row-count µs/call (extra detail), same cycling of copies
+    detail = {}
+    for rows in (1, 7, 16):
+        xr_ = x[:rows]
+        for name, fn in (("qkv_group", lambda i, xr_=xr_, rows=rows: tfx.group(sets[i % copies][:3], xr_, rows,
+                                                                               [y[:rows] for y in ys], stream)),
+                         ("single_5120", lambda i, xr_=xr_, rows=rows: tfx.linear(sets[i % copies][3], xr_, rows,
+                                                                                  yo[:rows], stream))):
+            for i in range(3):
+                fn(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            n_calls = max(20, args.steps)
+            for i in range(n_calls):
+                fn(i)
+            b.record(stream)
+            torch.cuda.synchronize()
+            detail[f"{name}_rows{rows}_us"] = round(a.elapsed_time(b) * 1e3 / n_calls, 3)
+    torch.cuda.synchronize()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = oracle_sample()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(sec_per_step * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "decode rows at 27B shapes: q/k/v group (6144+1024+1024) + single 5120x5120, "
+                                   "K=5120, 4-bit, 16 rows FP16",
+                       "K": K, "bits": BITS, "rows": ROWS, "weights_per_step_bytes": STEP_WEIGHT_BYTES,
+                       "l2": f"weights cycled through {copies} distinct copies "
+                             f"({copies * STEP_WEIGHT_BYTES / 1e6:.0f} MB > 4x L2)",
+                       "parallelism": f"replicas x{ws}"},
+            "us_per_step": round(sec_per_step * 1e6, 3),
+            "detail": detail,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "linear_kernel<4,2,8,4> (decode rows), group + single launch",
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel_us": {"group": round(grp_ms * 1e3, 3), "single": round(one_ms * 1e3, 3)}},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * 2,
+                    "d2h_bytes_per_step": sum(h.numel() * 2 for h in yh)},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("exl3_kernels.cuh", "exl3_host.cu", "exl3_bits.cu"):
+        h.update(open(os.path.join(ROOT, "exl3_trellis_quantized_rot_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

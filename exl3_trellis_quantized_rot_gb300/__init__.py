@@ -1,0 +1,231 @@
+"""Python binding of the tfx_exl3 C ABI (argument marshalling only).
+
+Every step of the layer runs in the CUDA kernels of ``libtfx_exl3.so``; this
+module only turns tensors into device pointers and streams into handles.
+If the library is missing the import of any entry point raises: there is no
+CPU fallback.
+
+Names follow the C ABI: ``linear``, ``group``, ``columns``, ``reserve``,
+``release``, ``reset_counters``, ``debug_decode``, ``plan``, ``stats``,
+``set_variant``, ``set_pdl``, ``last_error``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtfx_exl3.so")
+
+OK, EINVAL, ENOTRESERVED, EUNSUPPORTED, EALIGN, ECUDA = 0, -1, -2, -3, -4, -5
+F16, BF16 = 0, 1
+VARIANT_AUTO, VARIANT_ROWS, VARIANT_MID = 0, 1, 2
+
+ABI_SYMBOLS = ("tfx_exl3_linear", "tfx_exl3_group", "tfx_exl3_columns", "tfx_exl3_reserve",
+               "tfx_exl3_release", "tfx_exl3_reset_counters", "tfx_exl3_debug_decode", "tfx_exl3_plan",
+               "tfx_exl3_stats", "tfx_exl3_set_variant", "tfx_exl3_set_pdl", "tfx_exl3_debug_set_driver",
+               "tfx_exl3_debug_mark_events", "tfx_exl3_last_error")
+
+
+class WeightStruct(C.Structure):
+    _fields_ = [("trellis", C.c_void_p), ("suh", C.c_void_p), ("svh", C.c_void_p), ("K", C.c_int),
+                ("N", C.c_int), ("bits", C.c_int), ("tile_row_stride", C.c_int64), ("act", C.c_int),
+                ("priv", C.c_void_p)]
+
+
+ALLOC_FN = C.CFUNCTYPE(C.c_int, C.POINTER(C.c_void_p), C.c_size_t, C.c_void_p)
+FREE_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_void_p)
+MEMSET_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_size_t, C.c_void_p)
+
+
+class DriverStruct(C.Structure):
+    _fields_ = [("alloc", ALLOC_FN), ("free", FREE_FN), ("memset0", MEMSET_FN)]
+
+
+class TfxError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"tfx_exl3 error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libtfx_exl3.so (built by ``exl3_trellis_quantized_rot_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: run the build (python -m "
+                              "exl3_trellis_quantized_rot_gb300.build); there is no CPU fallback")
+        L = C.CDLL(LIB_PATH)
+        W = C.POINTER(WeightStruct)
+        vp, i = C.c_void_p, C.c_int
+        L.tfx_exl3_linear.argtypes = [W, vp, i, vp, vp]
+        L.tfx_exl3_group.argtypes = [C.POINTER(W), i, vp, i, C.POINTER(vp), vp]
+        L.tfx_exl3_columns.argtypes = [W, i, i, W]
+        L.tfx_exl3_reserve.argtypes = [W, i, vp]
+        L.tfx_exl3_release.argtypes = [W]
+        L.tfx_exl3_reset_counters.argtypes = [W, vp]
+        L.tfx_exl3_debug_decode.argtypes = [W, vp, vp]
+        L.tfx_exl3_plan.argtypes = [W, C.POINTER(i), C.POINTER(i)]
+        L.tfx_exl3_stats.argtypes = [W, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]
+        L.tfx_exl3_set_variant.argtypes = [i]
+        L.tfx_exl3_set_pdl.argtypes = [i]
+        L.tfx_exl3_debug_set_driver.argtypes = [C.POINTER(DriverStruct)]
+        L.tfx_exl3_debug_mark_events.argtypes = [vp, vp]
+        L.tfx_exl3_last_error.restype = C.c_char_p
+        for n in ABI_SYMBOLS[:-1]:
+            getattr(L, n).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().tfx_exl3_last_error().decode()
+
+
+def _check(rc: int) -> int:
+    if rc != 0:
+        raise TfxError(rc, last_error())
+    return rc
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else (t if isinstance(t, int) else t.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Weight:
+    """A quantized weight: the C descriptor plus references keeping its tensors alive.
+
+    trellis: uint32 words (int32 tensor), shape (K/16, tile_row_stride) or flat;
+    suh: K FP16; svh: N FP16; all on the same CUDA device (or raw pointers).
+    """
+
+    def __init__(self, trellis, suh, svh, K: int, N: int, bits: int, act: int = F16,
+                 tile_row_stride: int | None = None, _parent=None):
+        self.s = WeightStruct()
+        self.s.trellis, self.s.suh, self.s.svh = _ptr(trellis), _ptr(suh), _ptr(svh)
+        self.s.K, self.s.N, self.s.bits, self.s.act = K, N, bits, act
+        self.s.tile_row_stride = (N // 16) * 8 * bits if tile_row_stride is None else tile_row_stride
+        self.s.priv = None
+        self._keep = (trellis, suh, svh, _parent)
+
+    @property
+    def K(self):
+        return self.s.K
+
+    @property
+    def N(self):
+        return self.s.N
+
+    @property
+    def bits(self):
+        return self.s.bits
+
+    @property
+    def act(self):
+        return self.s.act
+
+    def ref(self):
+        return C.byref(self.s)
+
+    def __del__(self):
+        try:
+            if self.s.priv and _lib is not None:
+                _lib.tfx_exl3_release(C.byref(self.s))
+        except Exception:
+            pass
+
+
+def reserve(w: Weight, max_rows: int, stream=None) -> None:
+    _check(lib().tfx_exl3_reserve(w.ref(), max_rows, _stream(stream)))
+
+
+def release(w: Weight) -> None:
+    _check(lib().tfx_exl3_release(w.ref()))
+
+
+def reset_counters(w: Weight, stream=None) -> None:
+    _check(lib().tfx_exl3_reset_counters(w.ref(), _stream(stream)))
+
+
+def linear(w: Weight, x, rows: int | None = None, y=None, stream=None):
+    """y = layer(x); x is rows x K in the weight's act dtype. Returns y."""
+    import torch
+    if rows is None:
+        rows = x.shape[0]
+    if y is None:
+        y = torch.empty((rows, w.N), dtype=x.dtype, device=x.device)
+    _check(lib().tfx_exl3_linear(w.ref(), _ptr(x), rows, _ptr(y), _stream(stream)))
+    return y
+
+
+def group(ws, x, rows: int | None = None, ys=None, stream=None):
+    """One rotation and one launch over up to 3 weights of the same K. Returns ys."""
+    import torch
+    if rows is None:
+        rows = x.shape[0]
+    if ys is None:
+        ys = [torch.empty((rows, w.N), dtype=x.dtype, device=x.device) for w in ws]
+    n = len(ws)
+    arr = (C.POINTER(WeightStruct) * max(n, 1))(*[C.pointer(w.s) for w in ws])
+    yarr = (C.c_void_p * max(n, 1))(*[_ptr(y) for y in ys])
+    _check(lib().tfx_exl3_group(arr, n, _ptr(x), rows, yarr, _stream(stream)))
+    return ys
+
+
+def columns(w: Weight, start: int, n: int) -> Weight:
+    """View of whole 128-column blocks [start, start+n) sharing w's memory."""
+    v = Weight.__new__(Weight)
+    v.s = WeightStruct()
+    _check(lib().tfx_exl3_columns(w.ref(), start, n, C.byref(v.s)))
+    v._keep = (None, None, None, w)
+    return v
+
+
+def debug_decode(w: Weight, W_out=None, stream=None):
+    import torch
+    if W_out is None:
+        W_out = torch.empty((w.K, w.N), dtype=torch.float16, device="cuda")
+    _check(lib().tfx_exl3_debug_decode(w.ref(), _ptr(W_out), _stream(stream)))
+    return W_out
+
+
+def plan(w: Weight):
+    s, k = C.c_int(), C.c_int()
+    _check(lib().tfx_exl3_plan(w.ref(), C.byref(s), C.byref(k)))
+    return s.value, k.value
+
+
+def stats(w: Weight):
+    a, m = C.c_int64(), C.c_int64()
+    _check(lib().tfx_exl3_stats(w.ref(), C.byref(a), C.byref(m)))
+    return a.value, m.value
+
+
+def set_variant(v: int) -> int:
+    return lib().tfx_exl3_set_variant(v)
+
+
+def set_pdl(on: bool) -> int:
+    return lib().tfx_exl3_set_pdl(1 if on else 0)
+
+
+def mark_events(before, after) -> None:
+    """Record torch.cuda.Event `before`/`after` around the next call's linear kernel."""
+    _check(lib().tfx_exl3_debug_mark_events(before.cuda_event if before is not None else None,
+                                             after.cuda_event if after is not None else None))
+
+
+def set_driver(drv: DriverStruct | None) -> None:
+    _check(lib().tfx_exl3_debug_set_driver(C.byref(drv) if drv is not None else None))

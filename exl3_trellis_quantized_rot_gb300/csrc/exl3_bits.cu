@@ -1,0 +1,26 @@
+// Instantiates every kernel of one bit width; compiled once per width with
+// -DTFX_BITS=1..8 so the widths build in parallel.
+#include "exl3_kernels.cuh"
+
+#ifndef TFX_BITS
+#error "compile with -DTFX_BITS=<1..8>"
+#endif
+
+#define TFX_CAT2(a, b) a##b
+#define TFX_CAT(a, b) TFX_CAT2(a, b)
+
+namespace tfx {
+
+KernelSet TFX_CAT(kernels_b, TFX_BITS)() {
+  KernelSet k;
+  k.linear_rows[0] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 1, 8, 4>);
+  k.linear_rows[1] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 2, 8, 4>);
+  k.linear_mid[0] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 2, 16, 4>);
+  k.linear_mid[1] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 4, 16, 4>);
+  k.linear_mid[2] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 8, 16, 4>);
+  k.linear_mid[3] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 16, 16, 2>);
+  k.decode = reinterpret_cast<const void*>(&decode_kernel<TFX_BITS>);
+  return k;
+}
+
+}  // namespace tfx

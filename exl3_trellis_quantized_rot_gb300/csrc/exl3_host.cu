@@ -1,0 +1,465 @@
+// Host side of the tfx_exl3 C ABI: validation, plan, scratch reservation,
+// kernel choice and launches. No CPU fallback exists: every step of the
+// layer runs in the kernels of exl3_kernels.cuh.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "../../include/tfx_exl3.h"
+#include "exl3_kernels.cuh"
+
+namespace tfx {
+KernelSet kernels_b1();
+KernelSet kernels_b2();
+KernelSet kernels_b3();
+KernelSet kernels_b4();
+KernelSet kernels_b5();
+KernelSet kernels_b6();
+KernelSet kernels_b7();
+KernelSet kernels_b8();
+}  // namespace tfx
+
+namespace tfx {
+// Rotation of x for up to 3 sign vectors: xr_m = fp16(Hn(suh_m o x)) per
+// 128-block. One warp per (row, 128-block); x is read once.
+__global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArgs a) {
+  griddep_wait();
+  griddep_launch();
+  const int lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int nblk = a.K / 128;
+  if (item >= (long long)a.rows * nblk) return;
+  const long long r = item / nblk;
+  const int b = (int)(item % nblk);
+  const long long base = r * a.K + 128LL * b + 4 * lane;
+  float xv[4];
+  if (a.act == 0) {
+    uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(a.x) + base);
+    __half2 h0 = *reinterpret_cast<__half2*>(&u.x), h1 = *reinterpret_cast<__half2*>(&u.y);
+    xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
+  } else {
+    uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + base);
+    __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&u.x), h1 = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+    xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
+  }
+  for (int m = 0; m < a.count; m++) {
+    uint2 su = *reinterpret_cast<const uint2*>(a.suh[m] + 128LL * b + 4 * lane);
+    __half2 s0 = *reinterpret_cast<__half2*>(&su.x), s1 = *reinterpret_cast<__half2*>(&su.y);
+    float v[4] = {xv[0] * __low2float(s0), xv[1] * __high2float(s0), xv[2] * __low2float(s1),
+                  xv[3] * __high2float(s1)};
+    fwht128(v, lane);
+    __half2 o0 = __halves2half2(__float2half_rn(v[0] * kInvSqrt128), __float2half_rn(v[1] * kInvSqrt128));
+    __half2 o1 = __halves2half2(__float2half_rn(v[2] * kInvSqrt128), __float2half_rn(v[3] * kInvSqrt128));
+    uint2 out;
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(a.xr[m] + base) = out;
+  }
+}
+
+}  // namespace tfx
+
+namespace {
+using tfx::kRowsPerPass;
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(TFX_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- driver hooks
+
+int rt_alloc(void** p, size_t bytes, cudaStream_t s) { return cudaMallocAsync(p, bytes, s) == cudaSuccess ? 0 : -1; }
+int rt_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s) == cudaSuccess ? 0 : -1; }
+int rt_memset0(void* p, size_t bytes, cudaStream_t s) { return cudaMemsetAsync(p, 0, bytes, s) == cudaSuccess ? 0 : -1; }
+
+tfx_exl3_driver g_drv = {rt_alloc, rt_free, rt_memset0};
+
+int env_variant() {
+  const char* v = getenv("TFX_EXL3_VARIANT");
+  if (!v) return 0;
+  if (!strcmp(v, "rows")) return 1;
+  if (!strcmp(v, "mid")) return 2;
+  return 0;
+}
+int env_pdl() {
+  const char* v = getenv("TFX_EXL3_PDL");
+  return !(v && !strcmp(v, "0"));
+}
+int g_variant = env_variant();
+thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+int g_pdl = env_pdl();
+
+// ---------------------------------------------------------------- per-weight state
+
+struct Priv {
+  __half* xr = nullptr;
+  size_t xr_bytes = 0;
+  float* partial = nullptr;
+  size_t partial_bytes = 0;
+  int* counters = nullptr;
+  size_t counter_bytes = 0;
+  int max_rows = 0;
+  int64_t allocs = 0, memsets = 0;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate(const tfx_exl3_weight* w) {
+  if (!w) return fail(TFX_EINVAL, "null weight");
+  if (w->K <= 0 || w->N <= 0 || w->K % 128 || w->N % 128)
+    return fail(TFX_EINVAL, "K=%d and N=%d must be positive multiples of 128", w->K, w->N);
+  if (w->bits < 1 || w->bits > 8) return fail(TFX_EINVAL, "bits=%d outside 1..8", w->bits);
+  if (w->act != TFX_F16 && w->act != TFX_BF16) return fail(TFX_EINVAL, "act=%d", w->act);
+  if (!w->trellis || !w->suh || !w->svh) return fail(TFX_EINVAL, "null trellis/suh/svh");
+  if (w->tile_row_stride < (int64_t)(w->N / 16) * 8 * w->bits)
+    return fail(TFX_EINVAL, "tile_row_stride %lld below the weight's own %lld words",
+                (long long)w->tile_row_stride, (long long)(w->N / 16) * 8 * w->bits);
+  if (!aligned16(w->trellis) || !aligned16(w->suh) || !aligned16(w->svh))
+    return fail(TFX_EALIGN, "trellis/suh/svh must be 16-byte aligned");
+  return 0;
+}
+
+// One split from 64 blocks up, eight K slices (PR #1507 "What this changes":
+// plan() gives one split from 64 blocks up; the 3-block view planned eight
+// splits and four warps). Below 64 blocks: the smallest power of two S <= 8
+// with NB*S >= 64, lowered until each of the 4 slices of a split has >= 4 tiles.
+void plan_of(int K, int NB, int* S, int* Wk) {
+  const int TK = K / 16;
+  int s = 1, wk = 8;
+  if (NB < 64) {
+    wk = 4;
+    while (s < 8 && NB * s < 64) s *= 2;
+    while (s > 1 && TK / s < 4 * wk) s /= 2;
+  }
+  while (wk > 1 && wk > TK / s) wk /= 2;
+  *S = s;
+  *Wk = wk;
+}
+
+int passes_of(int rows) { return (rows + kRowsPerPass - 1) / kRowsPerPass; }
+
+struct Needs {
+  size_t xr, partial, counters;
+};
+
+Needs needs_of(const tfx_exl3_weight* w, int rows) {
+  int S, Wk;
+  plan_of(w->K, w->N / 128, &S, &Wk);
+  const int passes = passes_of(rows);
+  const int rp = rows < kRowsPerPass ? rows : kRowsPerPass;
+  Needs n;
+  n.xr = (size_t)rows * w->K * 2;
+  n.partial = (size_t)passes * S * rp * w->N * 4;
+  n.counters = (size_t)passes * (w->N / 128) * 4;
+  return n;
+}
+
+int grow(void** p, size_t* have, size_t want, cudaStream_t s, Priv* pv, bool zero) {
+  if (want <= *have) return 0;
+  void* np = nullptr;
+  if (g_drv.alloc(&np, want, s) != 0 || !np) return fail(TFX_ECUDA, "allocation of %zu bytes failed", want);
+  pv->allocs++;
+  if (zero) {
+    if (g_drv.memset0(np, want, s) != 0) return fail(TFX_ECUDA, "zeroing %zu bytes failed", want);
+    pv->memsets++;
+  }
+  if (*p) g_drv.free(*p, s);
+  *p = np;
+  *have = want;
+  return 0;
+}
+
+const tfx::KernelSet& kernels(int bits) {
+  static tfx::KernelSet ks[9];
+  static bool init = false;
+  if (!init) {
+    ks[1] = tfx::kernels_b1();
+    ks[2] = tfx::kernels_b2();
+    ks[3] = tfx::kernels_b3();
+    ks[4] = tfx::kernels_b4();
+    ks[5] = tfx::kernels_b5();
+    ks[6] = tfx::kernels_b6();
+    ks[7] = tfx::kernels_b7();
+    ks[8] = tfx::kernels_b8();
+    init = true;
+  }
+  return ks[bits];
+}
+
+int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void* arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (g_pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[1] = {arg};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return 0;
+}
+
+// The linear kernel family and its shape for `rows` rows.
+struct Family {
+  const void* fn;
+  int wpc, nr;
+};
+
+Family pick(int bits, int rows) {
+  const tfx::KernelSet& ks = kernels(bits);
+  const int prow = rows < kRowsPerPass ? rows : kRowsPerPass;
+  const bool rows_kernel = (g_variant == 1 || g_variant == 0) && rows <= 16;
+  if (rows_kernel) return prow <= 8 ? Family{ks.linear_rows[0], 8, 1} : Family{ks.linear_rows[1], 8, 2};
+  if (prow <= 16) return Family{ks.linear_mid[0], 16, 2};
+  if (prow <= 32) return Family{ks.linear_mid[1], 16, 4};
+  if (prow <= 64) return Family{ks.linear_mid[2], 16, 8};
+  return Family{ks.linear_mid[3], 16, 16};
+}
+
+int set_smem(const void* fn, size_t smem) {
+  if (smem <= 48 * 1024) return 0;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  return 0;
+}
+
+int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s) {
+  if (count < 1 || count > 3) return fail(TFX_EINVAL, "group count %d outside 1..3", count);
+  if (rows < 0) return fail(TFX_EINVAL, "rows=%d", rows);
+  if (!x || !ys) return fail(TFX_EINVAL, "null x or ys");
+  for (int i = 0; i < count; i++) {
+    int rc = validate(ws[i]);
+    if (rc) return rc;
+    if (!ys[i]) return fail(TFX_EINVAL, "null y of member %d", i);
+    if (!aligned16(ys[i])) return fail(TFX_EALIGN, "y of member %d is not 16-byte aligned", i);
+    if (ws[i]->K != ws[0]->K || ws[i]->bits != ws[0]->bits || ws[i]->act != ws[0]->act)
+      return fail(TFX_EUNSUPPORTED, "group members must share K, bits and act");
+  }
+  if (!aligned16(x)) return fail(TFX_EALIGN, "x is not 16-byte aligned");
+  if (rows == 0) return 0;
+  for (int i = 0; i < count; i++) {
+    const Priv* pv = static_cast<const Priv*>(ws[i]->priv);
+    if (!pv || pv->max_rows < rows)
+      return fail(TFX_ENOTRESERVED, "member %d reserved for %d rows, called with %d", i, pv ? pv->max_rows : 0,
+                  rows);
+  }
+  const int K = ws[0]->K, bits = ws[0]->bits;
+
+  // rotation of x, once for all members
+  tfx::RotArgs ra = {};
+  ra.x = x;
+  ra.count = count;
+  ra.rows = rows;
+  ra.K = K;
+  ra.act = ws[0]->act;
+  for (int i = 0; i < count; i++) {
+    ra.suh[i] = reinterpret_cast<const __half*>(ws[i]->suh);
+    ra.xr[i] = static_cast<Priv*>(ws[i]->priv)->xr;
+  }
+  const long long items = (long long)rows * (K / 128);
+  int rc = launch(reinterpret_cast<const void*>(&tfx::rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0,
+                  s, &ra);
+  if (rc) return rc;
+
+  // one grid over every member's CTAs
+  const Family f = pick(bits, rows);
+  tfx::LinearArgs la = {};
+  la.count = count;
+  la.K = K;
+  la.TK = K / 16;
+  la.rows = rows;
+  la.passes = passes_of(rows);
+  la.rp = rows < kRowsPerPass ? rows : kRowsPerPass;
+  la.act = ws[0]->act;
+  long long ctas = 0;
+  for (int i = 0; i < count; i++) {
+    const tfx_exl3_weight* w = ws[i];
+    Priv* pv = static_cast<Priv*>(w->priv);
+    tfx::Member& m = la.m[i];
+    m.trellis = w->trellis;
+    m.stride = w->tile_row_stride;
+    m.svh = reinterpret_cast<const __half*>(w->svh);
+    m.xr = pv->xr;
+    m.y = ys[i];
+    m.partial = pv->partial;
+    m.counters = pv->counters;
+    m.N = w->N;
+    m.NB = w->N / 128;
+    plan_of(K, m.NB, &m.S, &m.Wk);
+    m.TC = f.wpc / m.Wk;
+    if (m.TC > 8) m.TC = 8;
+    m.subs = 8 / m.TC;
+    m.cta_begin = (int)ctas;
+    ctas += (long long)m.NB * m.subs * m.S * la.passes;
+  }
+  if (ctas > 0x7fffffffLL) return fail(TFX_EUNSUPPORTED, "grid of %lld CTAs", ctas);
+  const size_t smem = (size_t)f.wpc * f.nr * 8 * 16 * sizeof(float);
+  rc = set_smem(f.fn, smem);
+  if (rc) return rc;
+  cudaEvent_t eb = g_ev_before, ea = g_ev_after;
+  g_ev_before = g_ev_after = nullptr;
+  if (eb && cudaEventRecord(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
+  rc = launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la);
+  if (rc) return rc;
+  if (ea && cudaEventRecord(ea, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tfx_exl3_linear(tfx_exl3_weight* w, const void* x, int rows, void* y, cudaStream_t stream) {
+  tfx_exl3_weight* ws[1] = {w};
+  void* ys[1] = {y};
+  return run(ws, 1, x, rows, ys, stream);
+}
+
+int tfx_exl3_group(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
+                   cudaStream_t stream) {
+  if (!ws) return fail(TFX_EINVAL, "null member list");
+  return run(ws, count, x, rows, ys, stream);
+}
+
+int tfx_exl3_columns(const tfx_exl3_weight* w, int from, int n, tfx_exl3_weight* view_out) {
+  int rc = validate(w);
+  if (rc) return rc;
+  if (!view_out) return fail(TFX_EINVAL, "null view_out");
+  if (from < 0 || n <= 0 || from % 128 || n % 128 || (long long)from + n > w->N)
+    return fail(TFX_EINVAL, "columns(from=%d, n=%d) is not a whole-block range of N=%d", from, n, w->N);
+  tfx_exl3_weight v = *w;
+  v.trellis = w->trellis + (long long)(from / 16) * 8 * w->bits;
+  v.svh = w->svh + from;
+  v.N = n;
+  v.priv = nullptr;
+  *view_out = v;
+  return 0;
+}
+
+int tfx_exl3_reserve(tfx_exl3_weight* w, int max_rows, cudaStream_t stream) {
+  int rc = validate(w);
+  if (rc) return rc;
+  if (max_rows < 1) return fail(TFX_EINVAL, "max_rows=%d", max_rows);
+  Priv* pv = static_cast<Priv*>(w->priv);
+  if (!pv) {
+    pv = new Priv();
+    w->priv = pv;
+  }
+  if (max_rows <= pv->max_rows) return 0;
+  const Needs nd = needs_of(w, max_rows);
+  rc = grow(reinterpret_cast<void**>(&pv->xr), &pv->xr_bytes, nd.xr, stream, pv, false);
+  if (!rc) rc = grow(reinterpret_cast<void**>(&pv->partial), &pv->partial_bytes, nd.partial, stream, pv, false);
+  if (!rc) rc = grow(reinterpret_cast<void**>(&pv->counters), &pv->counter_bytes, nd.counters, stream, pv, true);
+  if (rc) return rc;
+  pv->max_rows = max_rows;
+  return 0;
+}
+
+int tfx_exl3_release(tfx_exl3_weight* w) {
+  if (!w) return fail(TFX_EINVAL, "null weight");
+  Priv* pv = static_cast<Priv*>(w->priv);
+  if (!pv) return 0;
+  if (g_drv.alloc == rt_alloc) cudaDeviceSynchronize();
+  if (pv->xr) g_drv.free(pv->xr, nullptr);
+  if (pv->partial) g_drv.free(pv->partial, nullptr);
+  if (pv->counters) g_drv.free(pv->counters, nullptr);
+  if (g_drv.alloc == rt_alloc) cudaDeviceSynchronize();
+  delete pv;
+  w->priv = nullptr;
+  return 0;
+}
+
+int tfx_exl3_reset_counters(tfx_exl3_weight* w, cudaStream_t stream) {
+  if (!w) return fail(TFX_EINVAL, "null weight");
+  Priv* pv = static_cast<Priv*>(w->priv);
+  if (!pv || !pv->counters) return fail(TFX_ENOTRESERVED, "weight not reserved");
+  if (g_drv.memset0(pv->counters, pv->counter_bytes, stream) != 0) return fail(TFX_ECUDA, "zeroing counters");
+  pv->memsets++;
+  return 0;
+}
+
+int tfx_exl3_debug_decode(const tfx_exl3_weight* w, uint16_t* W_out, cudaStream_t stream) {
+  int rc = validate(w);
+  if (rc) return rc;
+  if (!W_out) return fail(TFX_EINVAL, "null W_out");
+  tfx::DecodeArgs da;
+  da.trellis = w->trellis;
+  da.stride = w->tile_row_stride;
+  da.W = reinterpret_cast<__half*>(W_out);
+  da.K = w->K;
+  da.N = w->N;
+  const long long tiles = (long long)(w->K / 16) * (w->N / 16);
+  return launch(kernels(w->bits).decode, dim3((unsigned)((tiles + 7) / 8)), dim3(256), 0, stream, &da);
+}
+
+int tfx_exl3_plan(const tfx_exl3_weight* w, int* splits, int* kslices) {
+  int rc = validate(w);
+  if (rc) return rc;
+  int S, Wk;
+  plan_of(w->K, w->N / 128, &S, &Wk);
+  if (splits) *splits = S;
+  if (kslices) *kslices = Wk;
+  return 0;
+}
+
+int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets) {
+  if (!w) return fail(TFX_EINVAL, "null weight");
+  const Priv* pv = static_cast<const Priv*>(w->priv);
+  if (allocs) *allocs = pv ? pv->allocs : 0;
+  if (memsets) *memsets = pv ? pv->memsets : 0;
+  return 0;
+}
+
+int tfx_exl3_set_variant(int variant) {
+  const int old = g_variant;
+  if (variant >= 0 && variant <= 2) g_variant = variant;
+  return old;
+}
+
+int tfx_exl3_set_pdl(int on) {
+  const int old = g_pdl;
+  g_pdl = on ? 1 : 0;
+  return old;
+}
+
+int tfx_exl3_debug_set_driver(const tfx_exl3_driver* d) {
+  if (!d) {
+    g_drv = tfx_exl3_driver{rt_alloc, rt_free, rt_memset0};
+    return 0;
+  }
+  if (!d->alloc || !d->free || !d->memset0) return fail(TFX_EINVAL, "driver hooks must all be set");
+  g_drv = *d;
+  return 0;
+}
+
+int tfx_exl3_debug_mark_events(cudaEvent_t before, cudaEvent_t after) {
+  g_ev_before = before;
+  g_ev_after = after;
+  return 0;
+}
+
+const char* tfx_exl3_last_error(void) { return g_err.c_str(); }
+
+}  // extern "C"

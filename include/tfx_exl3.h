@@ -1,0 +1,139 @@
+/*
+ * tfx_exl3 — EXL3 trellis-quantized, Hadamard-rotated linear layer for GB300 (sm_103a).
+ *
+ * C ABI. Every pointer to tensor data is a CUDA device pointer owned by the
+ * caller unless stated otherwise; the library never frees caller memory.
+ * Every call returns 0 on success or a negative TFX_E* code, never aborts,
+ * and on a validation error enqueues nothing. tfx_exl3_last_error() gives a
+ * thread-local message for the last failing call.
+ *
+ * The layer (TensorFold PR #1467 "exl3 cuda: the 27B's EXL3 speed series on
+ * the native Dense module", sections "What this changes" and "The arithmetic";
+ * PR #1407 item 2):
+ *     y = svh o Hn( fp16( Hn(suh o x) ) . W ),   Hn = H128 / sqrt(128) per 128-block
+ * where W (K x N) is decoded on the fly from `bits`-per-weight trellis codes
+ * stored in 16x16 tiles of 8*bits uint32 words, and the product is summed in
+ * FP32 with a deterministic split-K whose per-block arrival counters are reset
+ * by the last-arriving CTA (PR #1475 "exl3: zero the split-K counters once as
+ * they grow, not before every call", section "What this changes").
+ *
+ * Decode rule, tile layout and summation order: see the header comment of the
+ * kernels (exl3_trellis_quantized_rot_gb300/csrc/exl3_kernels.cuh).
+ */
+#ifndef TFX_EXL3_H
+#define TFX_EXL3_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define TFX_OK 0
+#define TFX_EINVAL -1        /* bad argument: shape, bits, count, null pointer */
+#define TFX_ENOTRESERVED -2  /* rows above the reserved capacity, or no reserve() yet */
+#define TFX_EUNSUPPORTED -3  /* valid but not served (e.g. group members of unequal K) */
+#define TFX_EALIGN -4        /* a pointer is not 16-byte aligned */
+#define TFX_ECUDA -5         /* a CUDA runtime call failed; see tfx_exl3_last_error() */
+
+typedef enum { TFX_F16 = 0, TFX_BF16 = 1 } tfx_dtype;
+
+/* A quantized weight. All pointers are caller-owned device memory.
+ * trellis : tiles of 8*bits uint32 words; tile (tk, tn) starts at word
+ *           tk*tile_row_stride + tn*8*bits, tk < K/16, tn < N/16. The 8 tiles
+ *           tn = 8*nb .. 8*nb+7 form 128-column block nb.
+ * suh     : K FP16 values (the input sign flips; any FP16 scale is allowed).
+ * svh     : N FP16 values (the output sign flips / scales).
+ * K, N    : multiples of 128. bits: 1..8.
+ * tile_row_stride : words between tile rows; (N/16)*8*bits for a full weight,
+ *           the parent's value for a column view.
+ * act     : dtype of x and y.
+ * priv    : library-owned state (scratch, counters), NULL until reserve(). */
+typedef struct {
+  const uint32_t* trellis;
+  const uint16_t* suh;
+  const uint16_t* svh;
+  int K, N, bits;
+  int64_t tile_row_stride;
+  int act;
+  void* priv;
+} tfx_exl3_weight;
+
+/* y[rows x N] = layer(x[rows x K]); x, y row-major in w->act, 16-byte aligned.
+ * rows == 0 is a no-op. rows above the reserved max_rows -> TFX_ENOTRESERVED.
+ * Enqueued on `stream`; allocates nothing and clears nothing (the counters
+ * are reset by the kernel itself). Calls on one weight must be ordered on
+ * one stream. Rows are cut into 128-row passes (PR #1475, "What this changes":
+ * counters indexed pass*NB + nb). */
+int tfx_exl3_linear(tfx_exl3_weight* w, const void* x, int rows, void* y, cudaStream_t stream);
+
+/* One rotation launch and one linear launch for up to 3 weights of the same
+ * K, bits and act over the same rows (PR #1467, "What this changes":
+ * matmulGroup runs up to three layers of one K over the same rows in one
+ * rotation and one launch). Each member keeps its own suh, svh, plan,
+ * scratch and counters; ys[i] is rows x ws[i]->N. Bytes equal those of
+ * tfx_exl3_linear on each member. count == 1 is tfx_exl3_linear. */
+int tfx_exl3_group(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
+                   cudaStream_t stream);
+
+/* A view of whole 128-column blocks [from, from+n) of w that reads the same
+ * stored words and keeps the parent's tile-row stride (PR #1507, "What this
+ * changes": exl3.Weight.columns(from, n)). from % 128 == 0, n % 128 == 0,
+ * from + n <= w->N. view_out->priv is NULL: reserve the view before use. */
+int tfx_exl3_columns(const tfx_exl3_weight* w, int from, int n, tfx_exl3_weight* view_out);
+
+/* Size the weight's scratch (rotated x, split-K partials, counters) for up
+ * to max_rows rows. Grows only; the counter buffer is zeroed on `stream`
+ * once per growth and never otherwise (PR #1475, "What this changes").
+ * Call before CUDA-graph capture; linear/group then allocate nothing. */
+int tfx_exl3_reserve(tfx_exl3_weight* w, int max_rows, cudaStream_t stream);
+
+/* Free priv (synchronises the device first). Safe on an unreserved weight. */
+int tfx_exl3_release(tfx_exl3_weight* w);
+
+/* Re-zero the counters on `stream` (recovery after a failed launch). */
+int tfx_exl3_reset_counters(tfx_exl3_weight* w, cudaStream_t stream);
+
+/* Write the decoded FP16 weight W (K x N, row-major W[k][n]) to W_out. */
+int tfx_exl3_debug_decode(const tfx_exl3_weight* w, uint16_t* W_out, cudaStream_t stream);
+
+/* The weight's K split and K slices per split; a pure function of (K, N/128).
+ * One split from 64 blocks up (PR #1507: plan() gives one split from 64
+ * blocks up, wide_blocks = 64). */
+int tfx_exl3_plan(const tfx_exl3_weight* w, int* splits, int* kslices);
+
+/* Allocations and counter memsets made for this weight since its creation. */
+int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
+
+/* Kernel family forced for the next calls: 0 = auto (1..16 rows decode-rows,
+ * more rows mid-rows), 1 = decode-rows whenever rows <= 16, 2 = mid-rows for
+ * every row count. The initial value comes from TFX_EXL3_VARIANT
+ * (auto|rows|mid). Returns the previous value. */
+int tfx_exl3_set_variant(int variant);
+
+/* Programmatic dependent launch on (1) or off (0); initial value from
+ * TFX_EXL3_PDL (default on). Returns the previous value. */
+int tfx_exl3_set_pdl(int on);
+
+/* Test hook: replace the allocator and memset used by reserve/release so the
+ * host logic runs without a GPU. NULL restores the CUDA runtime. */
+typedef struct {
+  int (*alloc)(void** p, size_t bytes, cudaStream_t s);
+  int (*free)(void* p, cudaStream_t s);
+  int (*memset0)(void* p, size_t bytes, cudaStream_t s);
+} tfx_exl3_driver;
+int tfx_exl3_debug_set_driver(const tfx_exl3_driver* d);
+
+/* Measurement hook: the next linear/group call on this thread records
+ * `before` just before its linear-kernel launch and `after` just after it,
+ * on the call's stream, then forgets both. Either may be NULL. */
+int tfx_exl3_debug_mark_events(cudaEvent_t before, cudaEvent_t after);
+
+const char* tfx_exl3_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TFX_EXL3_H */

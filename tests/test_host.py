@@ -1,0 +1,213 @@
+"""Host logic of the C ABI, run without a GPU.
+
+The allocator and memset of reserve/release are replaced by a counting fake
+(tfx_exl3_debug_set_driver) so the grow-only zeroing can be checked on CPU;
+every other check stops at validation, before any CUDA call.
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import exl3_trellis_quantized_rot_gb300 as tfx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    return tfx.lib()
+
+
+def header_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"\b(tfx_exl3_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = header_symbols()
+    assert "tfx_exl3_linear" in names and "tfx_exl3_group" in names
+    for n in sorted(names):
+        assert hasattr(L, n), n
+    assert set(tfx.ABI_SYMBOLS) <= names
+
+
+class FakeDriver:
+    """Counting stand-in for cudaMallocAsync / cudaFreeAsync / cudaMemsetAsync."""
+
+    def __init__(self):
+        self.allocs, self.frees, self.memsets = [], [], []
+        self.next = 1 << 20
+        self.s = tfx.DriverStruct(tfx.ALLOC_FN(self._alloc), tfx.FREE_FN(self._free), tfx.MEMSET_FN(self._memset))
+
+    def _alloc(self, pp, nbytes, stream):
+        p = self.next
+        self.next += (nbytes + 4095) // 4096 * 4096 + 4096
+        pp[0] = p
+        self.allocs.append((p, nbytes, stream))
+        return 0
+
+    def _free(self, p, stream):
+        self.frees.append((p, stream))
+        return 0
+
+    def _memset(self, p, nbytes, stream):
+        self.memsets.append((p, nbytes, stream))
+        return 0
+
+
+@pytest.fixture
+def drv(L):
+    d = FakeDriver()
+    tfx.set_driver(d.s)
+    yield d
+    tfx.set_driver(None)
+
+
+FAKE = 0x7F0000000000  # aligned stand-in device addresses (never dereferenced on the host)
+
+
+def fake_weight(K, N, bits, act=tfx.F16):
+    return tfx.Weight(FAKE, FAKE + (1 << 30), FAKE + (2 << 30), K, N, bits, act)
+
+
+def test_plan_rule(L):
+    # one split and eight K slices from 64 column blocks up
+    for N in (8192, 17408, 248320):
+        assert tfx.plan(fake_weight(5120, N, 4)) == (1, 8)
+    # the 3-block (384-column) view plans eight splits and four slices
+    assert tfx.plan(fake_weight(5120, 384, 6)) == (8, 4)
+    # the tiny layer takes one split
+    assert tfx.plan(fake_weight(256, 256, 4)) == (1, 4)
+    # 27B decode shapes
+    assert tfx.plan(fake_weight(5120, 5120, 4)) == (2, 4)
+    assert tfx.plan(fake_weight(5120, 6144, 4)) == (2, 4)
+    assert tfx.plan(fake_weight(5120, 1024, 4)) == (8, 4)
+    assert tfx.plan(fake_weight(17408, 5120, 4)) == (2, 4)
+    # rows and bits never enter the plan
+    assert tfx.plan(fake_weight(5120, 1024, 1)) == tfx.plan(fake_weight(5120, 1024, 8))
+    # small K keeps slices of whole tiles
+    s, k = tfx.plan(fake_weight(128, 256, 4))
+    assert s == 1 and 1 <= k <= 8
+
+
+def test_head_views_plan_like_the_head(L):
+    head = fake_weight(5120, 248320, 6)
+    first = tfx.columns(head, 0, 98304)
+    tail = tfx.columns(head, 240128, 8192)
+    assert tfx.plan(first) == tfx.plan(head) == tfx.plan(tail) == (1, 8)
+    # a 384-column tail would plan differently (the pages' red case)
+    assert tfx.plan(tfx.columns(head, 247936, 384)) != tfx.plan(head)
+
+
+def test_columns_view_keeps_strides_and_moves_to_first_block(L):
+    K, N, b = 512, 1024, 3
+    w = fake_weight(K, N, b)
+    v = tfx.columns(w, 256, 512)
+    assert v.s.tile_row_stride == w.s.tile_row_stride == (N // 16) * 8 * b
+    assert v.s.trellis == w.s.trellis + (256 // 16) * 8 * b * 4
+    assert v.s.svh == w.s.svh + 256 * 2
+    assert v.s.suh == w.s.suh and v.s.K == K and v.s.N == 512 and v.s.bits == b
+    assert not v.s.priv
+    # a view of a view composes
+    vv = tfx.columns(v, 128, 256)
+    assert vv.s.trellis == w.s.trellis + (384 // 16) * 8 * b * 4
+    for bad in [(1, 128), (0, 100), (896, 256), (-128, 128), (0, 0)]:
+        with pytest.raises(tfx.TfxError) as e:
+            tfx.columns(w, *bad)
+        assert e.value.code == tfx.EINVAL
+
+
+def test_reserve_grows_only_and_zeroes_counters_once_per_growth(L, drv):
+    w = fake_weight(5120, 5120, 4)
+    stream = 0x1234
+    tfx.reserve(w, 16, stream)
+    assert len(drv.allocs) == 3 and len(drv.memsets) == 1
+    cnt_ptr = drv.memsets[0][0]
+    assert drv.memsets[0][2] == stream  # on the call's stream, not the legacy stream
+    assert all(a[2] == stream for a in drv.allocs)
+    # counters: 1 pass x 40 blocks
+    assert drv.memsets[0][1] == 40 * 4 and cnt_ptr in [a[0] for a in drv.allocs]
+    # same or fewer rows: nothing
+    for r in (1, 7, 16):
+        tfx.reserve(w, r, stream)
+    assert len(drv.allocs) == 3 and len(drv.memsets) == 1
+    assert tfx.stats(w) == (3, 1)
+    # more rows within one pass: scratch grows, counters do not (still 1 pass)
+    tfx.reserve(w, 100, stream)
+    assert len(drv.memsets) == 1
+    # a second pass: the counter buffer grows and is zeroed once, on the stream
+    tfx.reserve(w, 200, 0x99)
+    assert len(drv.memsets) == 2 and drv.memsets[1][2] == 0x99 and drv.memsets[1][1] == 2 * 40 * 4
+    freed = {p for p, _ in drv.frees}
+    assert cnt_ptr in freed
+    tfx.release(w)
+    assert not w.s.priv
+
+
+def test_group_reserve_sizes_each_member(L, drv):
+    q, k, v = fake_weight(5120, 6144, 4), fake_weight(5120, 1024, 4), fake_weight(5120, 1024, 4)
+    for m in (q, k, v):
+        tfx.reserve(m, 16, 7)
+    n_alloc = len(drv.allocs)
+    # a reserved group call at 1..16 rows would allocate and zero nothing: reserve again is a no-op
+    for m in (q, k, v):
+        tfx.reserve(m, 16, 7)
+    assert len(drv.allocs) == n_alloc
+
+
+def test_validation_errors_before_any_launch(L, drv):
+    w = fake_weight(256, 256, 4)
+    x = FAKE + (3 << 30)
+    y = FAKE + (4 << 30)
+    # not reserved
+    assert L.tfx_exl3_linear(w.ref(), x, 1, y, None) == tfx.ENOTRESERVED
+    tfx.reserve(w, 8, 0)
+    assert L.tfx_exl3_linear(w.ref(), x, 9, y, None) == tfx.ENOTRESERVED
+    assert "reserved for 8" in tfx.last_error()
+    # rows == 0 is a no-op
+    assert L.tfx_exl3_linear(w.ref(), x, 0, y, None) == 0
+    assert L.tfx_exl3_linear(w.ref(), x, -1, y, None) == tfx.EINVAL
+    # alignment
+    assert L.tfx_exl3_linear(w.ref(), x + 2, 1, y, None) == tfx.EALIGN
+    assert L.tfx_exl3_linear(w.ref(), x, 1, y + 8, None) == tfx.EALIGN
+    # shapes and bits
+    for K, N, b in [(100, 256, 4), (256, 200, 4), (256, 256, 0), (256, 256, 9)]:
+        bad = fake_weight(K, N, b)
+        assert L.tfx_exl3_reserve(bad.ref(), 4, None) == tfx.EINVAL
+    # stride below the weight's own
+    bad = tfx.Weight(FAKE, FAKE, FAKE, 256, 256, 4, tile_row_stride=10)
+    assert L.tfx_exl3_plan(bad.ref(), None, None) == tfx.EINVAL
+    # group members must share K and bits; count within 1..3
+    a, b2 = fake_weight(256, 256, 4), fake_weight(512, 256, 4)
+    tfx.reserve(a, 4, 0)
+    tfx.reserve(b2, 4, 0)
+    arr = (C.POINTER(tfx.WeightStruct) * 2)(C.pointer(a.s), C.pointer(b2.s))
+    ys = (C.c_void_p * 2)(y, y)
+    assert L.tfx_exl3_group(arr, 2, x, 1, ys, None) == tfx.EUNSUPPORTED
+    assert L.tfx_exl3_group(arr, 4, x, 1, ys, None) == tfx.EINVAL
+    assert L.tfx_exl3_group(arr, 0, x, 1, ys, None) == tfx.EINVAL
+    # reset_counters on an unreserved weight
+    assert L.tfx_exl3_reset_counters(fake_weight(256, 256, 4).ref(), None) == tfx.ENOTRESERVED
+
+
+def test_reset_counters_goes_to_the_stream(L, drv):
+    w = fake_weight(256, 384, 2)
+    tfx.reserve(w, 4, 0x55)
+    tfx.reset_counters(w, 0x66)
+    assert drv.memsets[-1][2] == 0x66 and drv.memsets[-1][1] == 3 * 4
+    assert tfx.stats(w) == (3, 2)
+
+
+def test_variant_and_pdl_switches(L):
+    old = tfx.set_variant(tfx.VARIANT_MID)
+    assert tfx.set_variant(old) == tfx.VARIANT_MID
+    old = tfx.set_pdl(False)
+    assert tfx.set_pdl(old) == 0
