@@ -243,7 +243,18 @@ def run_gpu(args):
     ys = [torch.empty((ROWS, n), dtype=torch.float16, device=dev) for n in QKV]
     yo = torch.empty((ROWS, O_N), dtype=torch.float16, device=dev)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+    def event_pairs(n):
+        # torch creates the CUDA event lazily: record each once so its handle exists
+        out = []
+        for _ in range(n):
+            pr = []
+            for _ in range(2):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                b.record(stream)
+                pr.append((a, b))
+            out.append(pr)
+        return out
 
     def step(i, marks=None):
         q, k, v, o = sets[i % copies]
@@ -259,16 +270,15 @@ def run_gpu(args):
     torch.cuda.synchronize()
 
     # device-resident timing, with the linear kernels' own events on the launching stream
-    kern_pairs = []
+    kern_pairs = event_pairs(args.steps)
+    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         barrier(ws)
         torch.cuda.synchronize()
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(args.steps):
-            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
-            step(i, pairs)
-            kern_pairs.append(pairs)
+            step(i, kern_pairs[i])
         stop.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
