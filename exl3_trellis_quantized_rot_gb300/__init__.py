@@ -24,7 +24,7 @@ VARIANT_AUTO, VARIANT_ROWS, VARIANT_MID = 0, 1, 2
 ABI_SYMBOLS = ("tfx_exl3_linear", "tfx_exl3_group", "tfx_exl3_columns", "tfx_exl3_reserve",
                "tfx_exl3_release", "tfx_exl3_reset_counters", "tfx_exl3_debug_decode", "tfx_exl3_plan",
                "tfx_exl3_stats", "tfx_exl3_set_variant", "tfx_exl3_set_pdl", "tfx_exl3_debug_set_driver",
-               "tfx_exl3_debug_mark_events", "tfx_exl3_last_error")
+               "tfx_exl3_debug_mark_events", "tfx_exl3_linear_static", "tfx_exl3_last_error")
 
 
 class WeightStruct(C.Structure):
@@ -74,6 +74,7 @@ def lib() -> C.CDLL:
         L.tfx_exl3_set_pdl.argtypes = [i]
         L.tfx_exl3_debug_set_driver.argtypes = [C.POINTER(DriverStruct)]
         L.tfx_exl3_debug_mark_events.argtypes = [vp, vp]
+        L.tfx_exl3_linear_static.argtypes = [W, vp, i, vp, vp]
         L.tfx_exl3_last_error.restype = C.c_char_p
         for n in ABI_SYMBOLS[:-1]:
             getattr(L, n).restype = C.c_int
@@ -167,6 +168,19 @@ def linear(w: Weight, x, rows: int | None = None, y=None, stream=None):
     if y is None:
         y = torch.empty((rows, w.N), dtype=x.dtype, device=x.device)
     _check(lib().tfx_exl3_linear(w.ref(), _ptr(x), rows, _ptr(y), _stream(stream)))
+    return y
+
+
+def linear_static(w: Weight, x, rows: int | None = None, y=None, stream=None):
+    """tfx_exl3_linear with its scratch in the library's static device array:
+    for callers that cannot allocate device memory where they run the layer.
+    Needs no reserve(). Calls share the array: order them on one stream."""
+    import torch
+    if rows is None:
+        rows = x.shape[0]
+    if y is None:
+        y = torch.empty((rows, w.N), dtype=x.dtype, device=x.device)
+    _check(lib().tfx_exl3_linear_static(w.ref(), _ptr(x), rows, _ptr(y), _stream(stream)))
     return y
 
 

@@ -37,6 +37,7 @@ def _sources():
     jobs = [(os.path.join(CSRC, "exl3_bits.cu"), os.path.join(OUT, f"exl3_b{b}.o"), [f"-DTFX_BITS={b}"])
             for b in range(1, 9)]
     jobs.append((os.path.join(CSRC, "exl3_host.cu"), os.path.join(OUT, "exl3_host.o"), []))
+    jobs.append((os.path.join(CSRC, "exl3_noalloc.cu"), os.path.join(OUT, "exl3_noalloc.o"), []))
     return deps, jobs
 
 

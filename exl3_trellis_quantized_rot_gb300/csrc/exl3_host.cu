@@ -463,3 +463,9 @@ int tfx_exl3_debug_mark_events(cudaEvent_t before, cudaEvent_t after) {
 const char* tfx_exl3_last_error(void) { return g_err.c_str(); }
 
 }  // extern "C"
+
+// Internal hooks for the static-scratch entry point (exl3_noalloc.cu).
+namespace tfx {
+const void* rot_kernel_fn() { return reinterpret_cast<const void*>(&rot_kernel); }
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace tfx

@@ -84,6 +84,24 @@ int tfx_exl3_group(tfx_exl3_weight* const ws[], int count, const void* x, int ro
  * from + n <= w->N. view_out->priv is NULL: reserve the view before use. */
 int tfx_exl3_columns(const tfx_exl3_weight* w, int from, int n, tfx_exl3_weight* view_out);
 
+/* tfx_exl3_linear with no allocation at all: the rotated x, split-K partials
+ * and counters live in one static device array of 8 MiB built into the
+ * library (every GPU that loads the library keeps it until exit) instead of
+ * the memory tfx_exl3_reserve obtains. The pages have no counterpart of this
+ * call; it serves callers that cannot call cudaMalloc or any other allocator
+ * where they run the layer (code running inside a host callback or a context
+ * where allocation is forbidden, plugins whose host application owns all
+ * device memory, runtimes that must not allocate after start-up).
+ * w needs no reserve() (w->priv is ignored); x, y as for tfx_exl3_linear.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture. Each call
+ * zeroes the counters it uses with cudaMemsetAsync on `stream` (the array
+ * keeps what the previous call left). All calls share the one array: calls
+ * that overlap on the GPU race, so order them on one stream. A call whose
+ * scratch (counters + rows*K*2 + splits*min(rows,128)*N*4 bytes, rounded)
+ * exceeds the array returns TFX_EUNSUPPORTED with the sizes in the message. */
+int tfx_exl3_linear_static(const tfx_exl3_weight* w, const void* x, int rows, void* y, cudaStream_t stream);
+
 /* Size the weight's scratch (rotated x, split-K partials, counters) for up
  * to max_rows rows. Grows only; the counter buffer is zeroed on `stream`
  * once per growth and never otherwise (PR #1475, "What this changes").
