@@ -368,7 +368,7 @@ def run_gpu(args):
             "detail": detail,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "kernel": "linear_kernel<4,2,8,4> (decode rows), group + single launch",
+                         "kernel": "linear_rows_kernel<4,2,4,4> (decode rows), group + single launch",
                          "peak_source": f"{peak_kind} hbm_gbs",
                          "kernel_us": {"group": round(grp_ms * 1e3, 3), "single": round(one_ms * 1e3, 3)}},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * 2,

@@ -10,7 +10,7 @@
 #include <string>
 
 #include "../../include/tfx_exl3.h"
-#include "exl3_kernels.cuh"
+#include "exl3_internal.h"
 
 namespace tfx {
 KernelSet kernels_b1();
@@ -24,40 +24,51 @@ KernelSet kernels_b8();
 }  // namespace tfx
 
 namespace tfx {
-// Rotation of x for up to 3 sign vectors: xr_m = fp16(Hn(suh_m o x)) per
-// 128-block. One warp per (row, 128-block); x is read once.
+// Rotation of x for up to 3 sign vectors: xf_m = fp16(Hn(suh_m o x)) per
+// 128-block, written in B-fragment order (xf_index). One warp per
+// (row, 128-block); x is read once; rows rows..rows_pad-1 are written as zero.
 __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArgs a) {
   griddep_wait();
   griddep_launch();
   const int lane = threadIdx.x & 31;
   const long long item = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int nblk = a.K / 128;
-  if (item >= (long long)a.rows * nblk) return;
-  const long long r = item / nblk;
+  if (item >= (long long)a.rows_pad * nblk) return;
+  const int r = (int)(item / nblk);
   const int b = (int)(item % nblk);
-  const long long base = r * a.K + 128LL * b + 4 * lane;
-  float xv[4];
-  if (a.act == 0) {
-    uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(a.x) + base);
-    __half2 h0 = *reinterpret_cast<__half2*>(&u.x), h1 = *reinterpret_cast<__half2*>(&u.y);
-    xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
-  } else {
-    uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + base);
-    __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&u.x), h1 = *reinterpret_cast<__nv_bfloat162*>(&u.y);
-    xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
+  float xv[4] = {0.f, 0.f, 0.f, 0.f};
+  if (r < a.rows) {
+    const long long base = (long long)r * a.K + 128LL * b + 4 * lane;
+    if (a.act == 0) {
+      uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(a.x) + base);
+      __half2 h0 = *reinterpret_cast<__half2*>(&u.x), h1 = *reinterpret_cast<__half2*>(&u.y);
+      xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
+    } else {
+      uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + base);
+      __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&u.x), h1 = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+      xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
+    }
   }
+  // element k = 128b + 4*lane + e sits in tile 8b + lane/4 at kk = 4*(lane%4) + e;
+  // the pair (kk, kk+1) for kk = 4*(lane%4) + 2m belongs to fragment lane 4g + 2*(lane%2) + m,
+  // register (lane%4) >= 2 (the k+8 half)
+  const int TK = a.K / 16;
+  const int q = r >> 3, gq = r & 7;
+  const int tk = 8 * b + (lane >> 2);
+  const int reg = (lane & 3) >= 2 ? 1 : 0;
   for (int m = 0; m < a.count; m++) {
     uint2 su = *reinterpret_cast<const uint2*>(a.suh[m] + 128LL * b + 4 * lane);
     __half2 s0 = *reinterpret_cast<__half2*>(&su.x), s1 = *reinterpret_cast<__half2*>(&su.y);
     float v[4] = {xv[0] * __low2float(s0), xv[1] * __high2float(s0), xv[2] * __low2float(s1),
                   xv[3] * __high2float(s1)};
     fwht128(v, lane);
-    __half2 o0 = __halves2half2(__float2half_rn(v[0] * kInvSqrt128), __float2half_rn(v[1] * kInvSqrt128));
-    __half2 o1 = __halves2half2(__float2half_rn(v[2] * kInvSqrt128), __float2half_rn(v[3] * kInvSqrt128));
-    uint2 out;
-    out.x = *reinterpret_cast<uint32_t*>(&o0);
-    out.y = *reinterpret_cast<uint32_t*>(&o1);
-    *reinterpret_cast<uint2*>(a.xr[m] + base) = out;
+    uint32_t* out = reinterpret_cast<uint32_t*>(a.xf[m]);
+#pragma unroll
+    for (int mm = 0; mm < 2; mm++) {
+      __half2 h = __halves2half2(__float2half_rn(v[2 * mm] * kInvSqrt128), __float2half_rn(v[2 * mm + 1] * kInvSqrt128));
+      const int fl = 4 * gq + 2 * (lane & 1) + mm;
+      out[xf_index(q, tk, fl, TK) * 2 + reg] = *reinterpret_cast<uint32_t*>(&h);
+    }
   }
 }
 
@@ -108,8 +119,8 @@ int g_pdl = env_pdl();
 // ---------------------------------------------------------------- per-weight state
 
 struct Priv {
-  __half* xr = nullptr;
-  size_t xr_bytes = 0;
+  uint2* xf = nullptr;
+  size_t xf_bytes = 0;
   float* partial = nullptr;
   size_t partial_bytes = 0;
   int* counters = nullptr;
@@ -135,55 +146,45 @@ int validate(const tfx_exl3_weight* w) {
   return 0;
 }
 
-// One split from 64 blocks up, eight K slices (PR #1507 "What this changes":
-// plan() gives one split from 64 blocks up; the 3-block view planned eight
-// splits and four warps). Below 64 blocks: the smallest power of two S <= 8
-// with NB*S >= 64, lowered until each of the 4 slices of a split has >= 4 tiles.
-void plan_of(int K, int NB, int* S, int* Wk) {
-  const int TK = K / 16;
-  int s = 1, wk = 8;
-  if (NB < 64) {
-    wk = 4;
-    while (s < 8 && NB * s < 64) s *= 2;
-    while (s > 1 && TK / s < 4 * wk) s /= 2;
-  }
-  while (wk > 1 && wk > TK / s) wk /= 2;
-  *S = s;
-  *Wk = wk;
-}
-
 int passes_of(int rows) { return (rows + kRowsPerPass - 1) / kRowsPerPass; }
-
-struct Needs {
-  size_t xr, partial, counters;
-};
-
-Needs needs_of(const tfx_exl3_weight* w, int rows) {
-  int S, Wk;
-  plan_of(w->K, w->N / 128, &S, &Wk);
-  const int passes = passes_of(rows);
-  const int rp = rows < kRowsPerPass ? rows : kRowsPerPass;
-  Needs n;
-  n.xr = (size_t)rows * w->K * 2;
-  n.partial = (size_t)passes * S * rp * w->N * 4;
-  n.counters = (size_t)passes * (w->N / 128) * 4;
-  return n;
+int pow2ceil(long long v) {
+  int p = 1;
+  while (p < v) p *= 2;
+  return p;
 }
 
-int grow(void** p, size_t* have, size_t want, cudaStream_t s, Priv* pv, bool zero) {
-  if (want <= *have) return 0;
-  void* np = nullptr;
-  if (g_drv.alloc(&np, want, s) != 0 || !np) return fail(TFX_ECUDA, "allocation of %zu bytes failed", want);
-  pv->allocs++;
-  if (zero) {
-    if (g_drv.memset0(np, want, s) != 0) return fail(TFX_ECUDA, "zeroing %zu bytes failed", want);
-    pv->memsets++;
+// SMs of the current device (152 on GB300; also the answer when no device is visible).
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 152;
   }
-  if (*p) g_drv.free(*p, s);
-  *p = np;
-  *have = want;
-  return 0;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
+
+// Decode rows: chunks per warp, so that one launch is about TFX_ROWS_WAVE
+// warps per SM (launch shape only; the bits do not depend on it).
+#ifndef TFX_ROWS_WAVE
+#define TFX_ROWS_WAVE 32
+#endif
+int rows_group(int TN, int C) {
+  const long long units = (long long)TN * C, wave = (long long)sm_count() * TFX_ROWS_WAVE;
+  int g = pow2ceil((units + wave - 1) / wave);
+  const int cap = C < (1 << tfx::kRowsMaxLog2G) ? C : (1 << tfx::kRowsMaxLog2G);
+  return g < cap ? g : cap;
+}
+// Mid rows: chunks per 16-warp CTA.
+int mid_group(int C) { return C < 8 ? C : 8; }
 
 const tfx::KernelSet& kernels(int bits) {
   static tfx::KernelSet ks[9];
@@ -202,14 +203,14 @@ const tfx::KernelSet& kernels(int bits) {
   return ks[bits];
 }
 
-int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void* arg) {
+int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void* arg, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  if (g_pdl) {
+  if (pdl) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
@@ -221,31 +222,43 @@ int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, v
   return 0;
 }
 
-// The linear kernel family and its shape for `rows` rows.
+// The linear kernel family for `rows` rows.
 struct Family {
   const void* fn;
   int wpc, nr;
+  bool rows;  // the decode-rows kernel
 };
 
 Family pick(int bits, int rows) {
   const tfx::KernelSet& ks = kernels(bits);
   const int prow = rows < kRowsPerPass ? rows : kRowsPerPass;
-  const bool rows_kernel = (g_variant == 1 || g_variant == 0) && rows <= 16;
-  if (rows_kernel) return prow <= 8 ? Family{ks.linear_rows[0], 8, 1} : Family{ks.linear_rows[1], 8, 2};
-  if (prow <= 16) return Family{ks.linear_mid[0], 16, 2};
-  if (prow <= 32) return Family{ks.linear_mid[1], 16, 4};
-  if (prow <= 64) return Family{ks.linear_mid[2], 16, 8};
-  return Family{ks.linear_mid[3], 16, 16};
+  if (g_variant != 2 && rows <= 16)
+    return prow <= 8 ? Family{ks.linear_rows[0], tfx::kRowsWPC, 1, true}
+                     : Family{ks.linear_rows[1], tfx::kRowsWPC, 2, true};
+  if (prow <= 16) return Family{ks.linear_mid[0], 16, 2, false};
+  if (prow <= 32) return Family{ks.linear_mid[1], 16, 4, false};
+  if (prow <= 64) return Family{ks.linear_mid[2], 16, 8, false};
+  return Family{ks.linear_mid[3], 16, 16, false};
 }
 
+// Opt in to more than the default 48 KB of shared memory once per kernel and size.
 int set_smem(const void* fn, size_t smem) {
-  if (smem <= 48 * 1024) return 0;
+  static thread_local const void* last_fn[16] = {};
+  static thread_local size_t last_sz[16] = {};
+  if (smem < 32 * 1024) return 0;
+  for (int i = 0; i < 16; i++)
+    if (last_fn[i] == fn && last_sz[i] >= smem) return 0;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  static thread_local int next = 0;
+  last_fn[next] = fn;
+  last_sz[next] = smem;
+  next = (next + 1) % 16;
   return 0;
 }
 
-int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s) {
+// Validation of a call; on success every member is well formed and aligned.
+int validate_call(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[]) {
   if (count < 1 || count > 3) return fail(TFX_EINVAL, "group count %d outside 1..3", count);
   if (rows < 0) return fail(TFX_EINVAL, "rows=%d", rows);
   if (!x || !ys) return fail(TFX_EINVAL, "null x or ys");
@@ -258,34 +271,94 @@ int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* c
       return fail(TFX_EUNSUPPORTED, "group members must share K, bits and act");
   }
   if (!aligned16(x)) return fail(TFX_EALIGN, "x is not 16-byte aligned");
+  return 0;
+}
+
+int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s) {
+  int rc = validate_call(ws, count, x, rows, ys);
+  if (rc) return rc;
   if (rows == 0) return 0;
+  tfx::Scratch sc = {};
   for (int i = 0; i < count; i++) {
-    const Priv* pv = static_cast<const Priv*>(ws[i]->priv);
+    Priv* pv = static_cast<Priv*>(ws[i]->priv);
     if (!pv || pv->max_rows < rows)
       return fail(TFX_ENOTRESERVED, "member %d reserved for %d rows, called with %d", i, pv ? pv->max_rows : 0,
                   rows);
+    sc.xf[i] = pv->xf;
+    sc.partial[i] = pv->partial;
+    sc.counters[i] = pv->counters;
   }
+  return tfx::launch_layer(ws, count, x, rows, ys, s, sc, g_pdl != 0);
+}
+
+int grow(void** p, size_t* have, size_t want, cudaStream_t s, Priv* pv, bool zero) {
+  if (want <= *have) return 0;
+  void* np = nullptr;
+  if (g_drv.alloc(&np, want, s) != 0 || !np) return fail(TFX_ECUDA, "allocation of %zu bytes failed", want);
+  pv->allocs++;
+  if (zero) {
+    if (g_drv.memset0(np, want, s) != 0) return fail(TFX_ECUDA, "zeroing %zu bytes failed", want);
+    pv->memsets++;
+  }
+  if (*p) g_drv.free(*p, s);
+  *p = np;
+  *have = want;
+  return 0;
+}
+
+}  // namespace
+
+namespace tfx {
+
+int chunks_of(int K) {
+  const int TK = K / 16;
+  int c = 1;
+  while (c < kMaxChunks && 2 * c <= TK / 4) c *= 2;
+  return c;
+}
+
+size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows) { return (size_t)((rows + 7) / 8 * 8) * w->K * 2; }
+
+size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
+  const int C = chunks_of(w->K), TN = w->N / 16;
+  const int p_rows = C / rows_group(TN, C), p_mid = C / mid_group(C);
+  const int small = rows < 16 ? rows : 16;
+  size_t need = (size_t)(p_rows > p_mid ? p_rows : p_mid) * small * w->N * 4;
+  if (rows > 16) {
+    const size_t mid = (size_t)passes_of(rows) * p_mid * (rows < kRowsPerPass ? rows : kRowsPerPass) * w->N * 4;
+    if (mid > need) need = mid;
+  }
+  return need;
+}
+
+size_t counter_bytes_needed(const tfx_exl3_weight* w, int rows) {
+  return (size_t)passes_of(rows) * (w->N / 128) * sizeof(int);
+}
+
+int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s,
+                 const Scratch& sc, bool pdl) {
   const int K = ws[0]->K, bits = ws[0]->bits;
 
   // rotation of x, once for all members
-  tfx::RotArgs ra = {};
+  RotArgs ra = {};
   ra.x = x;
   ra.count = count;
   ra.rows = rows;
+  ra.rows_pad = (rows + 7) / 8 * 8;
   ra.K = K;
   ra.act = ws[0]->act;
   for (int i = 0; i < count; i++) {
     ra.suh[i] = reinterpret_cast<const __half*>(ws[i]->suh);
-    ra.xr[i] = static_cast<Priv*>(ws[i]->priv)->xr;
+    ra.xf[i] = sc.xf[i];
   }
-  const long long items = (long long)rows * (K / 128);
-  int rc = launch(reinterpret_cast<const void*>(&tfx::rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0,
-                  s, &ra);
+  const long long items = (long long)ra.rows_pad * (K / 128);
+  int rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
+                  pdl);
   if (rc) return rc;
 
   // one grid over every member's CTAs
   const Family f = pick(bits, rows);
-  tfx::LinearArgs la = {};
+  LinearArgs la = {};
   la.count = count;
   la.K = K;
   la.TK = K / 16;
@@ -296,38 +369,48 @@ int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* c
   long long ctas = 0;
   for (int i = 0; i < count; i++) {
     const tfx_exl3_weight* w = ws[i];
-    Priv* pv = static_cast<Priv*>(w->priv);
-    tfx::Member& m = la.m[i];
+    Member& m = la.m[i];
     m.trellis = w->trellis;
     m.stride = w->tile_row_stride;
     m.svh = reinterpret_cast<const __half*>(w->svh);
-    m.xr = pv->xr;
+    m.xf = sc.xf[i];
     m.y = ys[i];
-    m.partial = pv->partial;
-    m.counters = pv->counters;
+    m.partial = sc.partial[i];
+    m.counters = sc.counters[i];
     m.N = w->N;
     m.NB = w->N / 128;
-    plan_of(K, m.NB, &m.S, &m.Wk);
-    m.TC = f.wpc / m.Wk;
-    if (m.TC > 8) m.TC = 8;
-    m.subs = 8 / m.TC;
+    m.C = chunks_of(K);
     m.cta_begin = (int)ctas;
-    ctas += (long long)m.NB * m.subs * m.S * la.passes;
+    if (f.rows) {
+      const int TN = w->N / 16;
+      m.G = rows_group(TN, m.C);
+      m.TC = kRowsWPC;
+      m.P = m.C / m.G;
+      m.arrivals = (8 / kRowsWPC) * m.P;
+      ctas += (long long)(TN / kRowsWPC) * m.P;
+    } else {
+      m.G = mid_group(m.C);
+      m.TC = f.wpc / m.G > 8 ? 8 : f.wpc / m.G;
+      m.P = m.C / m.G;
+      m.arrivals = (8 / m.TC) * m.P;
+      ctas += (long long)m.NB * (8 / m.TC) * m.P * la.passes;
+    }
+    m.log2G = __builtin_ctz(m.G);
   }
   if (ctas > 0x7fffffffLL) return fail(TFX_EUNSUPPORTED, "grid of %lld CTAs", ctas);
-  const size_t smem = (size_t)f.wpc * f.nr * 8 * 16 * sizeof(float);
+  const size_t smem = f.rows ? 0 : (size_t)f.wpc * f.nr * 8 * 16 * sizeof(float);
   rc = set_smem(f.fn, smem);
   if (rc) return rc;
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && cudaEventRecord(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
-  rc = launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la);
+  rc = launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl);
   if (rc) return rc;
   if (ea && cudaEventRecord(ea, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
   return 0;
 }
 
-}  // namespace
+}  // namespace tfx
 
 extern "C" {
 
@@ -368,10 +451,13 @@ int tfx_exl3_reserve(tfx_exl3_weight* w, int max_rows, cudaStream_t stream) {
     w->priv = pv;
   }
   if (max_rows <= pv->max_rows) return 0;
-  const Needs nd = needs_of(w, max_rows);
-  rc = grow(reinterpret_cast<void**>(&pv->xr), &pv->xr_bytes, nd.xr, stream, pv, false);
-  if (!rc) rc = grow(reinterpret_cast<void**>(&pv->partial), &pv->partial_bytes, nd.partial, stream, pv, false);
-  if (!rc) rc = grow(reinterpret_cast<void**>(&pv->counters), &pv->counter_bytes, nd.counters, stream, pv, true);
+  rc = grow(reinterpret_cast<void**>(&pv->xf), &pv->xf_bytes, tfx::xf_bytes_needed(w, max_rows), stream, pv, false);
+  if (!rc)
+    rc = grow(reinterpret_cast<void**>(&pv->partial), &pv->partial_bytes, tfx::partial_bytes_needed(w, max_rows),
+              stream, pv, false);
+  if (!rc)
+    rc = grow(reinterpret_cast<void**>(&pv->counters), &pv->counter_bytes, tfx::counter_bytes_needed(w, max_rows),
+              stream, pv, true);
   if (rc) return rc;
   pv->max_rows = max_rows;
   return 0;
@@ -382,7 +468,7 @@ int tfx_exl3_release(tfx_exl3_weight* w) {
   Priv* pv = static_cast<Priv*>(w->priv);
   if (!pv) return 0;
   if (g_drv.alloc == rt_alloc) cudaDeviceSynchronize();
-  if (pv->xr) g_drv.free(pv->xr, nullptr);
+  if (pv->xf) g_drv.free(pv->xf, nullptr);
   if (pv->partial) g_drv.free(pv->partial, nullptr);
   if (pv->counters) g_drv.free(pv->counters, nullptr);
   if (g_drv.alloc == rt_alloc) cudaDeviceSynchronize();
@@ -411,16 +497,15 @@ int tfx_exl3_debug_decode(const tfx_exl3_weight* w, uint16_t* W_out, cudaStream_
   da.K = w->K;
   da.N = w->N;
   const long long tiles = (long long)(w->K / 16) * (w->N / 16);
-  return launch(kernels(w->bits).decode, dim3((unsigned)((tiles + 7) / 8)), dim3(256), 0, stream, &da);
+  return launch(kernels(w->bits).decode, dim3((unsigned)((tiles + 7) / 8)), dim3(256), 0, stream, &da, false);
 }
 
-int tfx_exl3_plan(const tfx_exl3_weight* w, int* splits, int* kslices) {
+int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk) {
   int rc = validate(w);
   if (rc) return rc;
-  int S, Wk;
-  plan_of(w->K, w->N / 128, &S, &Wk);
-  if (splits) *splits = S;
-  if (kslices) *kslices = Wk;
+  const int C = tfx::chunks_of(w->K);
+  if (chunks) *chunks = C;
+  if (tiles_per_chunk) *tiles_per_chunk = (w->K / 16) / C;
   return 0;
 }
 
@@ -464,8 +549,7 @@ const char* tfx_exl3_last_error(void) { return g_err.c_str(); }
 
 }  // extern "C"
 
-// Internal hooks for the static-scratch entry point (exl3_noalloc.cu).
+// Error reporting for the other C-ABI translation units.
 namespace tfx {
-const void* rot_kernel_fn() { return reinterpret_cast<const void*>(&rot_kernel); }
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
 }  // namespace tfx

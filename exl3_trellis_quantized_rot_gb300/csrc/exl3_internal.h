@@ -1,0 +1,30 @@
+// Internal interface between the C-ABI translation units (not installed).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+
+#include "../../include/tfx_exl3.h"
+#include "exl3_kernels.cuh"
+
+namespace tfx {
+
+// Scratch of one call, per member: rotated x (fragment order), subtree slabs, counters.
+struct Scratch {
+  uint2* xf[3];
+  float* partial[3];
+  int* counters[3];
+};
+
+// K chunks of the summation order: a pure function of K.
+int chunks_of(int K);
+// Bytes of rotated x, slabs and counters one weight needs for up to `rows` rows.
+size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows);
+size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows);
+size_t counter_bytes_needed(const tfx_exl3_weight* w, int rows);
+// Enqueue the rotation and the linear launch for validated members on `s`.
+int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s,
+                 const Scratch& sc, bool pdl);
+int report_error(int code, const char* msg);
+
+}  // namespace tfx

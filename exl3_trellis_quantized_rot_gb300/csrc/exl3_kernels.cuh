@@ -17,18 +17,23 @@
 //   output column n as the fragment row and k as the fragment column:
 //   n_local = g + 8*((i>>1)&1), k_local = 2t + (i&1) + 8*(i>>2), g = lane>>2,
 //   t = lane&3. Tile (tk, tn) starts at word tk*stride + tn*8*BITS.
-// Summation order (identical in every kernel variant, a function of K and the
-//   plan only): K is cut into S splits and each split into Wk slices of whole
-//   16-row tiles (contiguous, floor-divided). A slice is one chain of
-//   m16n8k16 MMAs from zero in increasing k. A split's partial is the FP32
-//   left fold of its slices in slice order; z is the left fold of the split
-//   partials in split order (PR #1467, "The arithmetic" and the maintainers'
-//   review: K ranges per warp, warp-order sums, split-order partials).
-// Split-K combine: each CTA writes its split partial to scratch, fences and
-//   increments the 128-column block's counter; the CTA that sees the last
-//   arrival folds the partials in split order, applies the output rotation
-//   and resets the counter to 0 (PR #1475, "What this changes": the last
-//   arriving program resets counters[pass*NB + nb]). No CTA ever waits.
+// Summation order (a function of K alone, identical in every kernel, launch
+//   shape, row count, group and column view): the K/16 tile rows are cut into
+//   C chunks, C a power of two, chunk c = tiles [c*TK/C, (c+1)*TK/C) (floor).
+//   A chunk's sum is one chain of m16n8k16 MMAs from zero in increasing k,
+//   accumulated in FP32. The C chunk sums combine by a balanced binary tree in
+//   chunk order: (c0+c1), (c2+c3), ... then pairs of those, up to the root.
+//   Any power-of-two group of consecutive chunks is a subtree, so a warp, a CTA
+//   or a set of CTAs (through the split-K scratch) can each own a subtree
+//   without changing a bit. The pages fix the determinism (PR #1467, "The
+//   arithmetic": the mid-M kernels keep the linear's K ranges, warp-order sums
+//   and split-order partials), not the tree shape.
+// Split-K combine: each CTA writes the sum of its subtree to a scratch slab,
+//   then one thread publishes it (fence + atomic increment of the 128-column
+//   block's counter). The CTA that sees the last arrival folds the slabs as a
+//   tree, applies the output rotation and svh, stores y and resets the counter
+//   to 0 (PR #1475, "What this changes": the last arriving program resets
+//   counters[pass*NB + nb]). No CTA ever waits on another.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -40,18 +45,22 @@ constexpr uint32_t kHashMul = 0x9E3779B1u;
 constexpr uint32_t kHashAdd = 0x7F4A7C15u;
 constexpr float kInvSqrt128 = 0.08838834764831845f;  // 1/sqrt(128) rounded to FP32
 constexpr int kRowsPerPass = 128;
+constexpr int kMaxChunks = 16;
 
 struct Member {
   const uint32_t* trellis;  // first tile of this weight (or view)
   long long stride;         // uint32 words between tile rows
   const __half* svh;        // N
-  const __half* xr;         // rotated x, rows x K, FP16
+  const uint2* xf;          // rotated x in B-fragment order (see xf_index)
   void* y;                  // rows x N, act dtype
-  float* partial;           // [pass][S][rp][N] FP32
+  float* partial;           // [pass][P][rp][N] FP32 subtree sums
   int* counters;            // [pass][NB]
-  int N, NB, S, Wk;         // plan
-  int TC;                   // 16-column tiles per CTA (= warps per CTA / Wk)
-  int subs;                 // CTAs per 128-column block per split (= 8 / TC)
+  int N, NB;
+  int C;                    // K chunks (power of two): defines the bits
+  int G, log2G;             // chunks per unit: a warp (decode rows) or a CTA (mid rows)
+  int P;                    // slabs per pass = C / G
+  int TC;                   // 16-column tiles per CTA
+  int arrivals;             // CTAs per (pass, 128-column block)
   int cta_begin;            // first blockIdx.x of this member
 };
 
@@ -68,8 +77,8 @@ struct LinearArgs {
 struct RotArgs {
   const void* x;        // rows x K, act dtype
   const __half* suh[3]; // per member
-  __half* xr[3];        // per member output
-  int count, rows, K, act;
+  uint2* xf[3];         // per member output, fragment order
+  int count, rows, rows_pad, K, act;  // rows_pad = rows rounded up to 8 (padding rows are zero)
 };
 
 struct DecodeArgs {
@@ -79,8 +88,56 @@ struct DecodeArgs {
   int K, N;
 };
 
+// The rotated x is stored in the order the m16n8k16 B operand is consumed:
+// for 8-row group q, 16-row tile tk of K and lane l = 4g + t, one uint2 holds
+// {x[8q+g][16tk+2t], x[8q+g][16tk+2t+1]} and {x[8q+g][16tk+2t+8], x[8q+g][16tk+2t+9]}.
+// A warp reads the fragment of one (q, tk) as 256 contiguous bytes.
+__host__ __device__ __forceinline__ long long xf_index(int q, int tk, int lane, int TK) {
+  return ((long long)q * TK + tk) * 32 + lane;
+}
+
+__host__ __device__ __forceinline__ int chunk_begin(int c, int TK, int C) { return (int)(((long long)c * TK) / C); }
+
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Balanced binary tree over n values in index order: (v0+v1), (v2+v3), ...
+template <int N>
+__device__ __forceinline__ float tree_sum(float (&v)[N]) {
+#pragma unroll
+  for (int step = 1; step < N; step *= 2) {
+#pragma unroll
+    for (int i = 0; i + step < N; i += 2 * step) v[i] = v[i] + v[i + step];
+  }
+  return v[0];
+}
+
+// Tree over n (a power of two <= 16) floats at p[i*stride]; CG selects L2 loads.
+template <bool CG>
+__device__ __forceinline__ float tree_load(const float* p, long long stride, int n) {
+  auto ld = [&](int i) { return CG ? __ldcg(p + i * stride) : p[i * stride]; };
+  if (n == 1) return ld(0);
+  if (n == 2) {
+    float v[2] = {ld(0), ld(1)};
+    return tree_sum<2>(v);
+  }
+  if (n == 4) {
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) v[i] = ld(i);
+    return tree_sum<4>(v);
+  }
+  if (n == 8) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = ld(i);
+    return tree_sum<8>(v);
+  }
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = ld(i);
+  return tree_sum<16>(v);
+}
 
 // Unnormalised 128-point Walsh-Hadamard transform (Sylvester order) of the
 // 128 values a warp holds, 4 per lane (element 4*lane + e). Fixed butterfly
@@ -107,10 +164,10 @@ __device__ __forceinline__ void fwht128(float (&v)[4], int lane) {
 // and 3 words above, counted from the word holding the first bit.
 template <int BITS>
 struct Geo {
-  static constexpr int kWords = 8 * BITS;             // words per tile
-  static constexpr int kRaw = BITS <= 4 ? 2 : 3;      // words loaded per lane
-  static constexpr int kSpan = 7 * BITS + 16;         // bits used after alignment
-  static constexpr int kNorm = (kSpan + 31) / 32;     // words after alignment
+  static constexpr int kWords = 8 * BITS;          // words per tile
+  static constexpr int kRaw = BITS <= 4 ? 2 : 3;   // words a lane needs
+  static constexpr int kSpan = 7 * BITS + 16;      // bits used after alignment
+  static constexpr int kNorm = (kSpan + 31) / 32;  // words after alignment
 };
 
 // Decode the lane's 8 weights from its (already bit-aligned) window into the
@@ -138,8 +195,7 @@ __device__ __forceinline__ void decode8(const uint32_t (&win)[Geo<BITS>::kNorm +
   }
 }
 
-// Load the raw words of the lane's window from a tile and align them so the
-// lane's first weight starts at bit 0.
+// Where a lane's window starts in a tile and how to align it to bit 0.
 template <int BITS>
 struct LaneWindow {
   int i0, i1, i2;  // word indices within the tile (circular)
@@ -182,132 +238,36 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// The linear: one CTA = (128-column block nb, column sub-tile, split s, pass);
-// warp (w, c) runs the chain of slice w over 16-column tile c of the CTA.
-// NR = 8-row MMA groups per pass handled (rows of the pass <= 8*NR);
-// WPC = warps per CTA; PF = tiles prefetched per warp.
-template <int BITS, int NR, int WPC, int PF>
-__global__ void __launch_bounds__(WPC * 32, (WPC <= 8 ? 4 : 1))
-    linear_kernel(const __grid_constant__ LinearArgs a) {
-  extern __shared__ float red[];  // [WPC][NR*8][16]
-  __shared__ int s_last;
-  griddep_wait();
-  griddep_launch();
-
-  int mi = 0;
-  if (a.count > 1 && (int)blockIdx.x >= a.m[1].cta_begin) mi = 1;
-  if (a.count > 2 && (int)blockIdx.x >= a.m[2].cta_begin) mi = 2;
-  const Member& M = a.m[mi];
-
-  int local = blockIdx.x - M.cta_begin;
-  const int pass = local % a.passes;
-  local /= a.passes;
-  const int s = local % M.S;
-  local /= M.S;
-  const int nb = local / M.subs, sub = local % M.subs;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int w = warp % M.Wk, c = warp / M.Wk;
-  const int tn = nb * 8 + sub * M.TC + c;
-
-  const int s0 = (s * a.TK) / M.S, s1 = ((s + 1) * a.TK) / M.S;
-  const int t0 = s0 + (w * (s1 - s0)) / M.Wk, t1 = s0 + ((w + 1) * (s1 - s0)) / M.Wk;
-  const int row0 = pass * kRowsPerPass;
-  const int prow = min(kRowsPerPass, a.rows - row0);
-
-  float acc[NR][4];
-#pragma unroll
-  for (int q = 0; q < NR; q++) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-
-  if (c < M.TC) {
-    LaneWindow<BITS> lw;
-    lw.init(lane);
-    const uint32_t* tp = M.trellis + (long long)t0 * M.stride + (long long)tn * (8 * BITS);
-    // x fragment pointers: row 8q+g, columns 16*tk + 2t (+8)
-    const uint32_t* xbase = reinterpret_cast<const uint32_t*>(M.xr + (long long)(row0 + g) * a.K + 16LL * t0 + 2 * t);
-    const long long xq = 4LL * a.K;  // 8 rows, in uint32 units
-    bool rv[NR];
-#pragma unroll
-    for (int q = 0; q < NR; q++) rv[q] = (8 * q + g) < prow;
-
-    const int ntiles = t1 - t0;
-    uint32_t ring[PF][Geo<BITS>::kRaw];
-#pragma unroll
-    for (int p = 0; p < PF; p++)
-      if (p < ntiles) lw.load(tp + (long long)p * M.stride, ring[p]);
-
-    for (int it = 0; it < ntiles; it += PF) {
-#pragma unroll
-      for (int p = 0; p < PF; p++) {
-        const int tk = it + p;
-        if (tk < ntiles) {
-          uint32_t win[Geo<BITS>::kNorm + 1];
-          lw.align(ring[p], win);
-          if (tk + PF < ntiles) lw.load(tp + (long long)(tk + PF) * M.stride, ring[p]);
-          uint32_t af[4];
-          decode8<BITS>(win, af);
-          const uint32_t* xp = xbase + 8LL * tk;
-#pragma unroll
-          for (int q = 0; q < NR; q++) {
-            uint32_t b0 = 0u, b1 = 0u;
-            if (rv[q]) {
-              b0 = __ldg(xp + q * xq);
-              b1 = __ldg(xp + q * xq + 4);
-            }
-            mma16816(acc[q], af, b0, b1);
-          }
-        }
-      }
-    }
-  }
-
-  // slice accumulators -> shared memory: red[warp][r][n_local]
-  float* rw = red + warp * (NR * 8 * 16);
-#pragma unroll
-  for (int q = 0; q < NR; q++) {
-    const int r0 = 8 * q + 2 * t;
-    rw[r0 * 16 + g] = acc[q][0];
-    rw[(r0 + 1) * 16 + g] = acc[q][1];
-    rw[r0 * 16 + g + 8] = acc[q][2];
-    rw[(r0 + 1) * 16 + g + 8] = acc[q][3];
-  }
-  __syncthreads();
-
-  // fold slices in slice order, write this split's partial for the CTA's columns
-  const int cols = M.TC * 16;
-  const long long slab = (long long)(pass * M.S + s) * a.rp;
-  float* part = M.partial;
-  for (int idx = threadIdx.x; idx < prow * cols; idx += WPC * 32) {
-    const int r = idx / cols, cc = idx - r * cols;
-    const int cw = cc >> 4, nl = cc & 15;
-    const float* src = red + (cw * M.Wk) * (NR * 8 * 16) + r * 16 + nl;
-    float v = src[0];
-    for (int ww = 1; ww < M.Wk; ww++) v += src[ww * (NR * 8 * 16)];
-    part[(slab + r) * M.N + (long long)(nb * 8 + sub * M.TC) * 16 + cc] = v;
-  }
-  __threadfence();
+// One thread publishes the CTA's slab (all threads wrote it before the barrier)
+// and learns whether it was the last arrival of the block. Release: fence then
+// relaxed atomic; acquire: fence after seeing the final count.
+__device__ __forceinline__ bool arrive_last(int* counter, int arrivals, int* s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int old = atomicAdd(&M.counters[pass * M.NB + nb], 1);
-    s_last = (old == M.S * M.subs - 1);
+    __threadfence();
+    const int old = atomicAdd(counter, 1);
+    const bool last = old == arrivals - 1;
+    if (last) __threadfence();
+    *s_flag = last;
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  return *s_flag != 0;
+}
 
-  // last arrival: fold splits in split order, rotate back, scale by svh, store y
+// Last arrival of a 128-column block: fold the P slabs as a tree, rotate back
+// (FWHT, 1/sqrt(128)), scale by svh and store y. One warp per row.
+__device__ __forceinline__ void block_epilogue(const Member& M, const LinearArgs& a, int pass, int nb, int prow,
+                                               int row0, int warp, int nwarps, int lane) {
   const int n0 = nb * 128 + 4 * lane;
   float sv[4];
 #pragma unroll
   for (int e = 0; e < 4; e++) sv[e] = __half2float(M.svh[n0 + e]);
-  for (int r = warp; r < prow; r += WPC) {
+  const long long slab = (long long)a.rp * M.N;
+  const float* base = M.partial + (long long)pass * M.P * slab + n0;
+  for (int r = warp; r < prow; r += nwarps) {
     float v[4];
 #pragma unroll
-    for (int e = 0; e < 4; e++) v[e] = __ldcg(part + ((long long)pass * M.S * a.rp + r) * M.N + n0 + e);
-    for (int ss = 1; ss < M.S; ss++) {
-#pragma unroll
-      for (int e = 0; e < 4; e++) v[e] += __ldcg(part + ((long long)(pass * M.S + ss) * a.rp + r) * M.N + n0 + e);
-    }
+    for (int e = 0; e < 4; e++) v[e] = tree_load<true>(base + (long long)r * M.N + e, slab, M.P);
     fwht128(v, lane);
 #pragma unroll
     for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
@@ -325,8 +285,291 @@ __global__ void __launch_bounds__(WPC * 32, (WPC <= 8 ? 4 : 1))
       *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(M.y) + yo) = out;
     }
   }
+}
+
+__device__ __forceinline__ const Member& pick_member(const LinearArgs& a) {
+  int mi = 0;
+  if (a.count > 1 && (int)blockIdx.x >= a.m[1].cta_begin) mi = 1;
+  if (a.count > 2 && (int)blockIdx.x >= a.m[2].cta_begin) mi = 2;
+  return a.m[mi];
+}
+
+// ---------------------------------------------------------------------------
+// Mid-rows kernel (any row count, 128-row passes). One CTA = TC tile-columns
+// x G chunks (one warp each, WPC = TC*G) of one chunk group s of one pass.
+// The CTA folds its G chunk sums as a tree in shared memory and writes slab s.
+// NR = 8-row MMA groups per pass (rows of the pass <= 8*NR); PF = tiles of
+// trellis words prefetched per warp.
+template <int BITS, int NR, int WPC, int PF>
+__global__ void __launch_bounds__(WPC * 32, (WPC <= 8 ? 4 : 1))
+    linear_kernel(const __grid_constant__ LinearArgs a) {
+  extern __shared__ float red[];  // [WPC][NR*8][16]
+  __shared__ int s_last;
+  griddep_wait();
+  griddep_launch();
+  const Member& M = pick_member(a);
+
+  int local = blockIdx.x - M.cta_begin;
+  const int pass = local % a.passes;
+  local /= a.passes;
+  const int s = local % M.P;
+  local /= M.P;
+  const int subs = 8 / M.TC;
+  const int nb = local / subs, sub = local % subs;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int w = warp % M.G, c = warp / M.G;
+  const int tn = nb * 8 + sub * M.TC + c;
+  const int chunk = s * M.G + w;
+  const int t0 = chunk_begin(chunk, a.TK, M.C), t1 = chunk_begin(chunk + 1, a.TK, M.C);
+  const int row0 = pass * kRowsPerPass;
+  const int prow = min(kRowsPerPass, a.rows - row0);
+
+  float acc[NR][4];
+#pragma unroll
+  for (int q = 0; q < NR; q++) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+
+  if (c < M.TC) {
+    LaneWindow<BITS> lw;
+    lw.init(lane);
+    const uint32_t* tp = M.trellis + (long long)t0 * M.stride + (long long)tn * (8 * BITS);
+    const uint2* xq = M.xf + xf_index(row0 / 8, t0, lane, a.TK);
+    const long long xstride_q = 32LL * a.TK;
+    const int ntiles = t1 - t0;
+    uint32_t ring[PF][Geo<BITS>::kRaw];
+#pragma unroll
+    for (int p = 0; p < PF; p++)
+      if (p < ntiles) lw.load(tp + (long long)p * M.stride, ring[p]);
+
+    for (int it = 0; it < ntiles; it += PF) {
+#pragma unroll
+      for (int p = 0; p < PF; p++) {
+        const int tk = it + p;
+        if (tk < ntiles) {
+          uint32_t win[Geo<BITS>::kNorm + 1];
+          lw.align(ring[p], win);
+          if (tk + PF < ntiles) lw.load(tp + (long long)(tk + PF) * M.stride, ring[p]);
+          uint32_t af[4];
+          decode8<BITS>(win, af);
+#pragma unroll
+          for (int q = 0; q < NR; q++) {
+            if (8 * q < prow) {
+              const uint2 bx = __ldg(xq + q * xstride_q + 32LL * tk);
+              mma16816(acc[q], af, bx.x, bx.y);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // chunk sums -> shared memory: red[warp][r][n_local]
+  float* rw = red + warp * (NR * 8 * 16);
+#pragma unroll
+  for (int q = 0; q < NR; q++) {
+    const int r0 = 8 * q + 2 * t;
+    rw[r0 * 16 + g] = acc[q][0];
+    rw[(r0 + 1) * 16 + g] = acc[q][1];
+    rw[r0 * 16 + g + 8] = acc[q][2];
+    rw[(r0 + 1) * 16 + g + 8] = acc[q][3];
+  }
+  __syncthreads();
+
+  // tree over the CTA's G chunks -> slab s of the CTA's columns
+  const int cols = M.TC * 16;
+  const long long slab = (long long)a.rp * M.N;
+  float* part = M.partial + ((long long)pass * M.P + s) * slab;
+  for (int idx = threadIdx.x; idx < prow * cols; idx += WPC * 32) {
+    const int r = idx / cols, cc = idx - r * cols;
+    const int cw = cc >> 4, nl = cc & 15;
+    const float* src = red + (cw * M.G) * (NR * 8 * 16) + r * 16 + nl;
+    part[(long long)r * M.N + (long long)(nb * 8 + sub * M.TC) * 16 + cc] =
+        tree_load<false>(src, NR * 8 * 16, M.G);
+  }
+  if (!arrive_last(&M.counters[pass * M.NB + nb], M.arrivals, &s_last)) return;
+  block_epilogue(M, a, pass, nb, prow, row0, warp, WPC, lane);
   __syncthreads();
   if (threadIdx.x == 0) M.counters[pass * M.NB + nb] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Decode-rows kernel (1..16 rows, one pass). One CTA = WPC warps = WPC
+// consecutive tile-columns of one 128-column block, all on the same chunk
+// group; each warp owns G consecutive chunks of its tile-column (a subtree),
+// runs their MMA chains one after the other and folds them in registers as the
+// tree prescribes (a binary counter of subtree sums). The subtree sum goes to
+// slab gidx. Small CTAs and a chunk grouping sized to the SM count keep the
+// work of one launch spread evenly over the GPU. Each lane prefetches the
+// trellis words and x fragments of the next PF tiles into registers; the word
+// loads skip L1, which keeps x resident there.
+
+// The words a lane needs from one tile. For BITS <= 4 a tile is at most 32
+// words: each lane loads one word (word l) and takes the words it needs from
+// their owners by shuffle. For BITS = 8 a lane loads words 2l, 2l+1 and takes
+// 2l+2 from lane l+1. Other widths load their 3 words directly.
+template <int BITS>
+struct WordFetch {
+  static constexpr int kOwn = BITS == 8 ? 2 : (BITS <= 4 ? 1 : Geo<BITS>::kRaw);
+  __device__ __forceinline__ static void load(const uint32_t* __restrict__ tile, const LaneWindow<BITS>& lw, int lane,
+                                              uint32_t (&own)[kOwn]) {
+    if constexpr (BITS <= 4) {
+      const int j = lane < 8 * BITS ? lane : 0;
+      asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(own[0]) : "l"(tile + j));
+    } else if constexpr (BITS == 8) {
+      uint2 v;
+      asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(tile + 2 * lane));
+      own[0] = v.x;
+      own[1] = v.y;
+    } else {
+      own[0] = __ldg(tile + lw.i0);
+      own[1] = __ldg(tile + lw.i1);
+      own[2] = __ldg(tile + lw.i2);
+    }
+  }
+  __device__ __forceinline__ static void gather(const uint32_t (&own)[kOwn], const LaneWindow<BITS>& lw, int lane,
+                                                uint32_t (&raw)[Geo<BITS>::kRaw]) {
+    if constexpr (BITS == 4) {
+      raw[0] = own[0];
+      raw[1] = __shfl_sync(0xffffffffu, own[0], (lane + 1) & 31);
+    } else if constexpr (BITS < 4) {
+      raw[0] = __shfl_sync(0xffffffffu, own[0], lw.i0);
+      raw[1] = __shfl_sync(0xffffffffu, own[0], lw.i1);
+    } else if constexpr (BITS == 8) {
+      raw[0] = own[0];
+      raw[1] = own[1];
+      raw[2] = __shfl_sync(0xffffffffu, own[0], (lane + 1) & 31);
+    } else {
+#pragma unroll
+      for (int i = 0; i < Geo<BITS>::kRaw; i++) raw[i] = own[i];
+    }
+  }
+};
+
+// One decode-rows step: the lane's words of one tile -> A fragment -> NR MMAs.
+template <int BITS, int NR>
+__device__ __forceinline__ void rows_step(const uint32_t (&own)[WordFetch<BITS>::kOwn], const uint2 (&xc)[NR],
+                                          const LaneWindow<BITS>& lw, int lane, float (&acc)[NR][4]) {
+  uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
+  WordFetch<BITS>::gather(own, lw, lane, raw);
+  lw.align(raw, win);
+  decode8<BITS>(win, af);
+#pragma unroll
+  for (int q = 0; q < NR; q++) mma16816(acc[q], af, xc[q].x, xc[q].y);
+}
+
+// The MMA chain of tiles [t0, t0+n) of one tile-column into acc (from zero).
+template <int BITS, int NR, int PF>
+__device__ __forceinline__ void rows_chain(const uint32_t* __restrict__ tp, long long wstride,
+                                           const uint2* __restrict__ xp, long long xstride_q, int n,
+                                           const LaneWindow<BITS>& lw, int lane, float (&acc)[NR][4]) {
+  using WF = WordFetch<BITS>;
+#pragma unroll
+  for (int q = 0; q < NR; q++) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+  uint32_t own[PF][WF::kOwn];
+  uint2 xr[PF][NR];
+#pragma unroll
+  for (int p = 0; p < PF; p++) {
+    if (p < n) {
+      WF::load(tp + p * wstride, lw, lane, own[p]);
+#pragma unroll
+      for (int q = 0; q < NR; q++) xr[p][q] = __ldg(xp + q * xstride_q + 32 * p);
+    }
+  }
+  int tk = 0;
+  // full rounds: every tile of the round exists, its refill may not
+  for (; tk + PF <= n; tk += PF) {
+#pragma unroll
+    for (int p = 0; p < PF; p++) {
+      uint32_t oc[WF::kOwn];
+      uint2 xc[NR];
+#pragma unroll
+      for (int i = 0; i < WF::kOwn; i++) oc[i] = own[p][i];
+#pragma unroll
+      for (int q = 0; q < NR; q++) xc[q] = xr[p][q];
+      const int nx = tk + p + PF;
+      if (nx < n) {
+        WF::load(tp + nx * wstride, lw, lane, own[p]);
+#pragma unroll
+        for (int q = 0; q < NR; q++) xr[p][q] = __ldg(xp + q * xstride_q + 32 * nx);
+      }
+      rows_step<BITS, NR>(oc, xc, lw, lane, acc);
+    }
+  }
+  // tail: the last n % PF tiles are already in registers
+#pragma unroll
+  for (int p = 0; p < PF; p++)
+    if (tk + p < n) rows_step<BITS, NR>(own[p], xr[p], lw, lane, acc);
+}
+
+constexpr int kRowsMaxLog2G = 3;  // up to 8 chunks per warp
+
+template <int BITS, int NR, int PF, int MINB, int WPC>
+__global__ void __launch_bounds__(WPC * 32, MINB) linear_rows_kernel(const __grid_constant__ LinearArgs a) {
+  __shared__ int s_last;
+  griddep_wait();
+  griddep_launch();
+  const Member& M = pick_member(a);
+
+  // one pass (rows <= 16): blockIdx -> (column group of WPC tile-columns, chunk group)
+  const int local = blockIdx.x - M.cta_begin;
+  const int gidx = local % M.P;
+  const int colgrp = local / M.P;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int tn = colgrp * WPC + warp;
+  const int nb = tn >> 3;
+  const int prow = a.rows;
+
+  LaneWindow<BITS> lw;
+  lw.init(lane);
+  const long long wstride = M.stride;
+  const long long xstride_q = 32LL * a.TK;
+  const uint32_t* col = M.trellis + (long long)tn * (8 * BITS);
+
+  // binary counter of subtree sums: level l (in shared memory, per warp and
+  // lane) holds a finished subtree of 2^l chunks until its right sibling is done
+  __shared__ float lev[WPC][kRowsMaxLog2G][NR * 4][32];
+  float acc[NR][4];
+  for (int ci = 0; ci < M.G; ci++) {
+    const int chunk = gidx * M.G + ci;
+    const int t0 = chunk_begin(chunk, a.TK, M.C), t1 = chunk_begin(chunk + 1, a.TK, M.C);
+    rows_chain<BITS, NR, PF>(col + (long long)t0 * wstride, wstride, M.xf + xf_index(0, t0, lane, a.TK), xstride_q,
+                             t1 - t0, lw, lane, acc);
+    // while bit l of ci is set: acc = lev[l] + acc; then park acc at the first clear bit
+    int l = 0;
+    for (; l < kRowsMaxLog2G && ((ci >> l) & 1); l++) {
+#pragma unroll
+      for (int q = 0; q < NR; q++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) acc[q][e] = lev[warp][l][q * 4 + e][lane] + acc[q][e];
+    }
+    if (ci + 1 < M.G) {
+#pragma unroll
+      for (int q = 0; q < NR; q++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) lev[warp][l][q * 4 + e][lane] = acc[q][e];
+    }
+  }
+  // after the last chunk acc holds the whole subtree of G chunks
+
+  // subtree sum -> slab gidx: lane (g, t) holds (n = g | g+8, r = 8q + 2t | +1)
+  float* part = M.partial + (long long)gidx * a.rp * M.N + tn * 16;
+#pragma unroll
+  for (int q = 0; q < NR; q++) {
+    const int r0 = 8 * q + 2 * t;
+    if (r0 < prow) {
+      part[(long long)r0 * M.N + g] = acc[q][0];
+      part[(long long)r0 * M.N + g + 8] = acc[q][2];
+    }
+    if (r0 + 1 < prow) {
+      part[(long long)(r0 + 1) * M.N + g] = acc[q][1];
+      part[(long long)(r0 + 1) * M.N + g + 8] = acc[q][3];
+    }
+  }
+  if (!arrive_last(&M.counters[nb], M.arrivals, &s_last)) return;
+  block_epilogue(M, a, 0, nb, prow, 0, warp, WPC, lane);
+  __syncthreads();
+  if (threadIdx.x == 0) M.counters[nb] = 0;
 }
 
 // Debug: decode every tile to W[k][n] (FP16). One warp per tile.
@@ -356,9 +599,13 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ Dec
   }
 }
 
-// Kernel pointers for one bit width (defined in exl3_b<BITS>.cu).
+// Kernel pointers for one bit width (defined in exl3_bits.cu).
+#ifndef TFX_ROWS_WPC
+#define TFX_ROWS_WPC 2
+#endif
+constexpr int kRowsWPC = TFX_ROWS_WPC;  // warps (tile-columns) per decode-rows CTA
 struct KernelSet {
-  const void* linear_rows[2];  // decode-rows family: NR = 1, 2 (8 warps)
+  const void* linear_rows[2];  // decode-rows family: NR = 1, 2
   const void* linear_mid[4];   // mid-rows family: NR = 2, 4, 8, 16 (16 warps)
   const void* decode;
 };

@@ -117,10 +117,14 @@ int tfx_exl3_reset_counters(tfx_exl3_weight* w, cudaStream_t stream);
 /* Write the decoded FP16 weight W (K x N, row-major W[k][n]) to W_out. */
 int tfx_exl3_debug_decode(const tfx_exl3_weight* w, uint16_t* W_out, cudaStream_t stream);
 
-/* The weight's K split and K slices per split; a pure function of (K, N/128).
- * One split from 64 blocks up (PR #1507: plan() gives one split from 64
- * blocks up, wide_blocks = 64). */
-int tfx_exl3_plan(const tfx_exl3_weight* w, int* splits, int* kslices);
+/* The summation plan: K is cut into *chunks (a power of two <= 16, at least
+ * 4 tiles of 16 rows each, *tiles_per_chunk = (K/16)/chunks rounded down) whose
+ * FP32 MMA-chain sums combine by a balanced binary tree in chunk order. A pure
+ * function of K: rows, N, views, groups and launch shapes never change it, so
+ * a column view always gives the bytes of the same columns of its parent
+ * (PR #1507 needed its tail view to take 64 blocks so that plan() gave it the
+ * head's K split). */
+int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk);
 
 /* Allocations and counter memsets made for this weight since its creation. */
 int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);

@@ -47,7 +47,7 @@ def test_tiny_layer_matches_oracle():
     x64, x = x_of(0, 1, 256)
     y = tfx.linear(w, x)
     assert_close(to_f64(y), oracle_y(hw, x64), what="tiny")
-    assert tfx.plan(w) == (1, 4)
+    assert tfx.plan(w) == (4, 4)
 
 
 # ------------------------------------------------------------------ config 2
@@ -209,7 +209,7 @@ def test_lm_head_views_equal_full_head():
     tail = tfx.columns(w, 240128, 8192)
     tfx.reserve(first, 16)
     tfx.reserve(tail, 16)
-    assert tfx.plan(first) == tfx.plan(tail) == tfx.plan(w) == (1, 8)
+    assert tfx.plan(first) == tfx.plan(tail) == tfx.plan(w) == (16, 20)
     for rows in (1, 8, 16):
         x64, x = x_of(11, rows, K)
         full = tfx.linear(w, x)

@@ -79,32 +79,26 @@ def fake_weight(K, N, bits, act=tfx.F16):
 
 
 def test_plan_rule(L):
-    # one split and eight K slices from 64 column blocks up
-    for N in (8192, 17408, 248320):
-        assert tfx.plan(fake_weight(5120, N, 4)) == (1, 8)
-    # the 3-block (384-column) view plans eight splits and four slices
-    assert tfx.plan(fake_weight(5120, 384, 6)) == (8, 4)
-    # the tiny layer takes one split
-    assert tfx.plan(fake_weight(256, 256, 4)) == (1, 4)
-    # 27B decode shapes
-    assert tfx.plan(fake_weight(5120, 5120, 4)) == (2, 4)
-    assert tfx.plan(fake_weight(5120, 6144, 4)) == (2, 4)
-    assert tfx.plan(fake_weight(5120, 1024, 4)) == (8, 4)
-    assert tfx.plan(fake_weight(17408, 5120, 4)) == (2, 4)
-    # rows and bits never enter the plan
+    # the plan is the number of K chunks whose tree-ordered sum defines the bits:
+    # a power of two <= 16 with at least 4 tiles per chunk; rows, N and bits never enter
+    for N in (128, 384, 1024, 5120, 8192, 17408, 248320):
+        assert tfx.plan(fake_weight(5120, N, 4)) == (16, 20)
+    assert tfx.plan(fake_weight(17408, 5120, 4)) == (16, 68)
+    assert tfx.plan(fake_weight(256, 256, 4)) == (4, 4)
+    assert tfx.plan(fake_weight(128, 256, 4)) == (2, 4)
     assert tfx.plan(fake_weight(5120, 1024, 1)) == tfx.plan(fake_weight(5120, 1024, 8))
-    # small K keeps slices of whole tiles
-    s, k = tfx.plan(fake_weight(128, 256, 4))
-    assert s == 1 and 1 <= k <= 8
+    for K in range(128, 20000, 128):
+        C, tiles = tfx.plan(fake_weight(K, 256, 4))
+        assert C & (C - 1) == 0 and 1 <= C <= 16 and (K // 16) // C >= 4
+        assert C == 16 or 2 * C > (K // 16) // 4
 
 
 def test_head_views_plan_like_the_head(L):
+    # the pages' tail view had to take 64 blocks so that it planned like the head;
+    # here the plan depends on K alone, so every whole-block view plans like its parent
     head = fake_weight(5120, 248320, 6)
-    first = tfx.columns(head, 0, 98304)
-    tail = tfx.columns(head, 240128, 8192)
-    assert tfx.plan(first) == tfx.plan(head) == tfx.plan(tail) == (1, 8)
-    # a 384-column tail would plan differently (the pages' red case)
-    assert tfx.plan(tfx.columns(head, 247936, 384)) != tfx.plan(head)
+    for start, n in [(0, 98304), (240128, 8192), (247936, 384), (128, 128)]:
+        assert tfx.plan(tfx.columns(head, start, n)) == tfx.plan(head)
 
 
 def test_columns_view_keeps_strides_and_moves_to_first_block(L):
