@@ -10,19 +10,19 @@
 #define TFX_CAT(a, b) TFX_CAT2(a, b)
 
 // Launch-shape constants of the decode-rows kernel: prefetch depth and the
-// minimum resident 2-warp CTAs per SM (16 -> 64 registers, 12 -> 80) for
+// minimum resident 8-warp CTAs per SM (4 -> 64 registers, 3 -> 80) for
 // 1..8 and 9..16 rows.
 #ifndef TFX_ROWS_PF1
 #define TFX_ROWS_PF1 4
 #endif
 #ifndef TFX_ROWS_MINB1
-#define TFX_ROWS_MINB1 (TFX_BITS == 7 ? 12 : 16)
+#define TFX_ROWS_MINB1 ((TFX_BITS >= 5 && TFX_BITS <= 7) ? 3 : 4)
 #endif
 #ifndef TFX_ROWS_PF2
-#define TFX_ROWS_PF2 ((TFX_BITS >= 5 && TFX_BITS <= 7) ? 2 : 4)
+#define TFX_ROWS_PF2 (TFX_BITS == 4 ? 4 : 2)
 #endif
 #ifndef TFX_ROWS_MINB2
-#define TFX_ROWS_MINB2 12
+#define TFX_ROWS_MINB2 3
 #endif
 
 namespace tfx {
@@ -30,9 +30,9 @@ namespace tfx {
 KernelSet TFX_CAT(kernels_b, TFX_BITS)() {
   KernelSet k;
   k.linear_rows[0] =
-      reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 1, TFX_ROWS_PF1, TFX_ROWS_MINB1, kRowsWPC>);
+      reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 1, TFX_ROWS_PF1, TFX_ROWS_MINB1>);
   k.linear_rows[1] =
-      reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 2, TFX_ROWS_PF2, TFX_ROWS_MINB2, kRowsWPC>);
+      reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 2, TFX_ROWS_PF2, TFX_ROWS_MINB2>);
   k.linear_mid[0] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 2, 16, 4>);
   k.linear_mid[1] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 4, 16, 4>);
   k.linear_mid[2] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 8, 16, 4>);

@@ -172,16 +172,18 @@ int sm_count() {
   return cached[dev];
 }
 
-// Decode rows: chunks per warp, so that one launch is about TFX_ROWS_WAVE
-// warps per SM (launch shape only; the bits do not depend on it).
-#ifndef TFX_ROWS_WAVE
-#define TFX_ROWS_WAVE 32
-#endif
+// Decode rows: warp groups per column (GW) and chunks per warp (G). GW*G
+// chunks form one CTA's subtree; G grows while the launch keeps at least
+// 4 CTAs per SM (launch shape only; the bits do not depend on it).
+int rows_gw(int C) { return C < tfx::kRowsGW ? C : tfx::kRowsGW; }
 int rows_group(int TN, int C) {
-  const long long units = (long long)TN * C, wave = (long long)sm_count() * TFX_ROWS_WAVE;
-  int g = pow2ceil((units + wave - 1) / wave);
-  const int cap = C < (1 << tfx::kRowsMaxLog2G) ? C : (1 << tfx::kRowsMaxLog2G);
-  return g < cap ? g : cap;
+  const int gw = rows_gw(C);
+  const long long want = 4LL * sm_count();
+  int g = 1;
+  while (2 * g <= (1 << tfx::kRowsMaxLog2G) && gw * 2 * g <= C &&
+         (long long)(TN / tfx::kRowsTC) * (C / (gw * 2 * g)) >= want)
+    g *= 2;
+  return g;
 }
 // Mid rows: chunks per 16-warp CTA.
 int mid_group(int C) { return C < 8 ? C : 8; }
@@ -233,8 +235,8 @@ Family pick(int bits, int rows) {
   const tfx::KernelSet& ks = kernels(bits);
   const int prow = rows < kRowsPerPass ? rows : kRowsPerPass;
   if (g_variant != 2 && rows <= 16)
-    return prow <= 8 ? Family{ks.linear_rows[0], tfx::kRowsWPC, 1, true}
-                     : Family{ks.linear_rows[1], tfx::kRowsWPC, 2, true};
+    return prow <= 8 ? Family{ks.linear_rows[0], tfx::kRowsTC * tfx::kRowsGW, 1, true}
+                     : Family{ks.linear_rows[1], tfx::kRowsTC * tfx::kRowsGW, 2, true};
   if (prow <= 16) return Family{ks.linear_mid[0], 16, 2, false};
   if (prow <= 32) return Family{ks.linear_mid[1], 16, 4, false};
   if (prow <= 64) return Family{ks.linear_mid[2], 16, 8, false};
@@ -321,7 +323,7 @@ size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows) { return (size_t)((ro
 
 size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
   const int C = chunks_of(w->K), TN = w->N / 16;
-  const int p_rows = C / rows_group(TN, C), p_mid = C / mid_group(C);
+  const int p_rows = C / (rows_gw(C) * rows_group(TN, C)), p_mid = C / mid_group(C);
   const int small = rows < 16 ? rows : 16;
   size_t need = (size_t)(p_rows > p_mid ? p_rows : p_mid) * small * w->N * 4;
   if (rows > 16) {
@@ -384,10 +386,10 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     if (f.rows) {
       const int TN = w->N / 16;
       m.G = rows_group(TN, m.C);
-      m.TC = kRowsWPC;
-      m.P = m.C / m.G;
-      m.arrivals = (8 / kRowsWPC) * m.P;
-      ctas += (long long)(TN / kRowsWPC) * m.P;
+      m.TC = rows_gw(m.C);  // the decode-rows kernel reads its warp-group count here
+      m.P = m.C / (m.TC * m.G);
+      m.arrivals = (8 / kRowsTC) * m.P;
+      ctas += (long long)(TN / kRowsTC) * m.P;
     } else {
       m.G = mid_group(m.C);
       m.TC = f.wpc / m.G > 8 ? 8 : f.wpc / m.G;

@@ -502,69 +502,81 @@ __device__ __forceinline__ void rows_chain(const uint32_t* __restrict__ tp, long
 }
 
 constexpr int kRowsMaxLog2G = 3;  // up to 8 chunks per warp
+constexpr int kRowsTC = 2;        // tile-columns per decode-rows CTA
+constexpr int kRowsGW = 4;        // warp groups per tile-column (consecutive chunk groups)
 
-template <int BITS, int NR, int PF, int MINB, int WPC>
-__global__ void __launch_bounds__(WPC * 32, MINB) linear_rows_kernel(const __grid_constant__ LinearArgs a) {
+// CTA = kRowsTC x kRowsGW warps; warp (c, h) owns chunks [(gidx*GW + h)*G, +G)
+// of tile-column c. Warp trees (registers + parked levels in shared memory),
+// then a tree over the GW warps of a column in shared memory, give the CTA's
+// subtree of GW*G chunks: slab gidx of P = C/(GW*G).
+template <int BITS, int NR, int PF, int MINB>
+__global__ void __launch_bounds__(kRowsTC * kRowsGW * 32, MINB)
+    linear_rows_kernel(const __grid_constant__ LinearArgs a) {
+  constexpr int WPC = kRowsTC * kRowsGW;
   __shared__ int s_last;
+  __shared__ float lev[WPC][kRowsMaxLog2G][NR * 4][32];
+  __shared__ float red[kRowsTC][kRowsGW][NR * 8][16];
   griddep_wait();
   griddep_launch();
   const Member& M = pick_member(a);
 
-  // one pass (rows <= 16): blockIdx -> (column group of WPC tile-columns, chunk group)
+  // one pass (rows <= 16): blockIdx -> (column group of kRowsTC tile-columns, chunk group)
   const int local = blockIdx.x - M.cta_begin;
   const int gidx = local % M.P;
   const int colgrp = local / M.P;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int tn = colgrp * WPC + warp;
+  const int c = warp % kRowsTC, h = warp / kRowsTC;
+  const int tn = colgrp * kRowsTC + c;
   const int nb = tn >> 3;
   const int prow = a.rows;
+  const int GW = M.TC;  // warp groups in use (kRowsGW, or C when C < kRowsGW)
 
-  LaneWindow<BITS> lw;
-  lw.init(lane);
-  const long long wstride = M.stride;
-  const long long xstride_q = 32LL * a.TK;
-  const uint32_t* col = M.trellis + (long long)tn * (8 * BITS);
-
-  // binary counter of subtree sums: level l (in shared memory, per warp and
-  // lane) holds a finished subtree of 2^l chunks until its right sibling is done
-  __shared__ float lev[WPC][kRowsMaxLog2G][NR * 4][32];
-  float acc[NR][4];
-  for (int ci = 0; ci < M.G; ci++) {
-    const int chunk = gidx * M.G + ci;
-    const int t0 = chunk_begin(chunk, a.TK, M.C), t1 = chunk_begin(chunk + 1, a.TK, M.C);
-    rows_chain<BITS, NR, PF>(col + (long long)t0 * wstride, wstride, M.xf + xf_index(0, t0, lane, a.TK), xstride_q,
-                             t1 - t0, lw, lane, acc);
-    // while bit l of ci is set: acc = lev[l] + acc; then park acc at the first clear bit
-    int l = 0;
-    for (; l < kRowsMaxLog2G && ((ci >> l) & 1); l++) {
+  if (h < GW) {
+    LaneWindow<BITS> lw;
+    lw.init(lane);
+    const long long wstride = M.stride;
+    const long long xstride_q = 32LL * a.TK;
+    const uint32_t* col = M.trellis + (long long)tn * (8 * BITS);
+    float acc[NR][4];
+    for (int ci = 0; ci < M.G; ci++) {
+      const int chunk = (gidx * GW + h) * M.G + ci;
+      const int t0 = chunk_begin(chunk, a.TK, M.C), t1 = chunk_begin(chunk + 1, a.TK, M.C);
+      rows_chain<BITS, NR, PF>(col + (long long)t0 * wstride, wstride, M.xf + xf_index(0, t0, lane, a.TK),
+                               xstride_q, t1 - t0, lw, lane, acc);
+      // while bit l of ci is set: acc = lev[l] + acc; then park acc at the first clear bit
+      int l = 0;
+      for (; l < kRowsMaxLog2G && ((ci >> l) & 1); l++) {
 #pragma unroll
-      for (int q = 0; q < NR; q++)
+        for (int q = 0; q < NR; q++)
 #pragma unroll
-        for (int e = 0; e < 4; e++) acc[q][e] = lev[warp][l][q * 4 + e][lane] + acc[q][e];
+          for (int e = 0; e < 4; e++) acc[q][e] = lev[warp][l][q * 4 + e][lane] + acc[q][e];
+      }
+      if (ci + 1 < M.G) {
+#pragma unroll
+        for (int q = 0; q < NR; q++)
+#pragma unroll
+          for (int e = 0; e < 4; e++) lev[warp][l][q * 4 + e][lane] = acc[q][e];
+      }
     }
-    if (ci + 1 < M.G) {
+    // warp subtree -> red[c][h]: lane (g, t) holds (n = g | g+8, r = 8q + 2t | +1)
 #pragma unroll
-      for (int q = 0; q < NR; q++)
-#pragma unroll
-        for (int e = 0; e < 4; e++) lev[warp][l][q * 4 + e][lane] = acc[q][e];
+    for (int q = 0; q < NR; q++) {
+      const int r0 = 8 * q + 2 * t;
+      red[c][h][r0][g] = acc[q][0];
+      red[c][h][r0 + 1][g] = acc[q][1];
+      red[c][h][r0][g + 8] = acc[q][2];
+      red[c][h][r0 + 1][g + 8] = acc[q][3];
     }
   }
-  // after the last chunk acc holds the whole subtree of G chunks
+  __syncthreads();
 
-  // subtree sum -> slab gidx: lane (g, t) holds (n = g | g+8, r = 8q + 2t | +1)
-  float* part = M.partial + (long long)gidx * a.rp * M.N + tn * 16;
-#pragma unroll
-  for (int q = 0; q < NR; q++) {
-    const int r0 = 8 * q + 2 * t;
-    if (r0 < prow) {
-      part[(long long)r0 * M.N + g] = acc[q][0];
-      part[(long long)r0 * M.N + g + 8] = acc[q][2];
-    }
-    if (r0 + 1 < prow) {
-      part[(long long)(r0 + 1) * M.N + g] = acc[q][1];
-      part[(long long)(r0 + 1) * M.N + g + 8] = acc[q][3];
-    }
+  // tree over the GW warp subtrees of each column -> slab gidx
+  float* part = M.partial + (long long)gidx * a.rp * M.N + colgrp * (kRowsTC * 16);
+  for (int idx = threadIdx.x; idx < prow * kRowsTC * 16; idx += WPC * 32) {
+    const int r = idx / (kRowsTC * 16), cc = idx % (kRowsTC * 16);
+    const int cw = cc >> 4, nl = cc & 15;
+    part[(long long)r * M.N + cc] = tree_load<false>(&red[cw][0][r][nl], NR * 8 * 16, GW);
   }
   if (!arrive_last(&M.counters[nb], M.arrivals, &s_last)) return;
   block_epilogue(M, a, 0, nb, prow, 0, warp, WPC, lane);
@@ -600,10 +612,6 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ Dec
 }
 
 // Kernel pointers for one bit width (defined in exl3_bits.cu).
-#ifndef TFX_ROWS_WPC
-#define TFX_ROWS_WPC 2
-#endif
-constexpr int kRowsWPC = TFX_ROWS_WPC;  // warps (tile-columns) per decode-rows CTA
 struct KernelSet {
   const void* linear_rows[2];  // decode-rows family: NR = 1, 2
   const void* linear_mid[4];   // mid-rows family: NR = 2, 4, 8, 16 (16 warps)
