@@ -24,7 +24,8 @@ VARIANT_AUTO, VARIANT_ROWS, VARIANT_MID = 0, 1, 2
 ABI_SYMBOLS = ("tfx_exl3_linear", "tfx_exl3_group", "tfx_exl3_columns", "tfx_exl3_reserve",
                "tfx_exl3_release", "tfx_exl3_reset_counters", "tfx_exl3_debug_decode", "tfx_exl3_plan",
                "tfx_exl3_stats", "tfx_exl3_set_variant", "tfx_exl3_set_pdl", "tfx_exl3_debug_set_driver",
-               "tfx_exl3_debug_mark_events", "tfx_exl3_linear_static", "tfx_exl3_last_error")
+               "tfx_exl3_debug_mark_events", "tfx_exl3_linear_static", "tfx_exl3_debug_error",
+               "tfx_exl3_last_error")
 
 
 class WeightStruct(C.Structure):
@@ -75,6 +76,7 @@ def lib() -> C.CDLL:
         L.tfx_exl3_debug_set_driver.argtypes = [C.POINTER(DriverStruct)]
         L.tfx_exl3_debug_mark_events.argtypes = [vp, vp]
         L.tfx_exl3_linear_static.argtypes = [W, vp, i, vp, vp]
+        L.tfx_exl3_debug_error.argtypes = [W, C.POINTER(i)]
         L.tfx_exl3_last_error.restype = C.c_char_p
         for n in ABI_SYMBOLS[:-1]:
             getattr(L, n).restype = C.c_int
@@ -225,6 +227,13 @@ def stats(w: Weight):
     a, m = C.c_int64(), C.c_int64()
     _check(lib().tfx_exl3_stats(w.ref(), C.byref(a), C.byref(m)))
     return a.value, m.value
+
+
+def device_error(w: Weight) -> int:
+    """1 if a tensor-core launch on w gave up a bounded wait, else 0."""
+    e = C.c_int()
+    _check(lib().tfx_exl3_debug_error(w.ref(), C.byref(e)))
+    return e.value
 
 
 def set_variant(v: int) -> int:

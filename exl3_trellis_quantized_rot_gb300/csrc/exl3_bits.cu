@@ -1,6 +1,7 @@
 // Instantiates every kernel of one bit width; compiled once per width with
 // -DTFX_BITS=1..8 so the widths build in parallel.
 #include "exl3_kernels.cuh"
+#include "exl3_tc.cuh"
 
 #ifndef TFX_BITS
 #error "compile with -DTFX_BITS=<1..8>"
@@ -33,10 +34,7 @@ KernelSet TFX_CAT(kernels_b, TFX_BITS)() {
       reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 1, TFX_ROWS_PF1, TFX_ROWS_MINB1>);
   k.linear_rows[1] =
       reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 2, TFX_ROWS_PF2, TFX_ROWS_MINB2>);
-  k.linear_mid[0] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 2, 16, 4>);
-  k.linear_mid[1] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 4, 16, 4>);
-  k.linear_mid[2] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 8, 16, 4>);
-  k.linear_mid[3] = reinterpret_cast<const void*>(&linear_kernel<TFX_BITS, 16, 16, 2>);
+  k.linear_tc = reinterpret_cast<const void*>(&linear_tc_kernel<TFX_BITS>);
   k.decode = reinterpret_cast<const void*>(&decode_kernel<TFX_BITS>);
   return k;
 }

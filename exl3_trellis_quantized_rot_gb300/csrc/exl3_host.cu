@@ -11,6 +11,7 @@
 
 #include "../../include/tfx_exl3.h"
 #include "exl3_internal.h"
+#include "exl3_tc.cuh"
 
 namespace tfx {
 KernelSet kernels_b1();
@@ -25,7 +26,8 @@ KernelSet kernels_b8();
 
 namespace tfx {
 // Rotation of x for up to 3 sign vectors: xf_m = fp16(Hn(suh_m o x)) per
-// 128-block, written in B-fragment order (xf_index). One warp per
+// 128-block, written in B-fragment order (xf_index) for the decode-rows kernel
+// or in core-matrix order (xc_byte) for the tensor-core kernel. One warp per
 // (row, 128-block); x is read once; rows rows..rows_pad-1 are written as zero.
 __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArgs a) {
   griddep_wait();
@@ -62,12 +64,23 @@ __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArg
     float v[4] = {xv[0] * __low2float(s0), xv[1] * __high2float(s0), xv[2] * __low2float(s1),
                   xv[3] * __high2float(s1)};
     fwht128(v, lane);
-    uint32_t* out = reinterpret_cast<uint32_t*>(a.xf[m]);
+    __half2 h[2];
 #pragma unroll
-    for (int mm = 0; mm < 2; mm++) {
-      __half2 h = __halves2half2(__float2half_rn(v[2 * mm] * kInvSqrt128), __float2half_rn(v[2 * mm + 1] * kInvSqrt128));
-      const int fl = 4 * gq + 2 * (lane & 1) + mm;
-      out[xf_index(q, tk, fl, TK) * 2 + reg] = *reinterpret_cast<uint32_t*>(&h);
+    for (int mm = 0; mm < 2; mm++)
+      h[mm] = __halves2half2(__float2half_rn(v[2 * mm] * kInvSqrt128), __float2half_rn(v[2 * mm + 1] * kInvSqrt128));
+    if (a.layout == 0) {
+      uint32_t* out = reinterpret_cast<uint32_t*>(a.xf[m]);
+#pragma unroll
+      for (int mm = 0; mm < 2; mm++) {
+        const int fl = 4 * gq + 2 * (lane & 1) + mm;
+        out[xf_index(q, tk, fl, TK) * 2 + reg] = *reinterpret_cast<uint32_t*>(&h[mm]);
+      }
+    } else {
+      // the lane's 4 values are k%8 = 4*(lane%2) .. +3 of one core-matrix row: one 8-byte store
+      uint2 o;
+      o.x = *reinterpret_cast<uint32_t*>(&h[0]);
+      o.y = *reinterpret_cast<uint32_t*>(&h[1]);
+      *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(a.xf[m]) + xc_byte(r, 128 * b + 4 * lane, a.rows_pad / 8)) = o;
     }
   }
 }
@@ -146,12 +159,6 @@ int validate(const tfx_exl3_weight* w) {
   return 0;
 }
 
-int passes_of(int rows) { return (rows + kRowsPerPass - 1) / kRowsPerPass; }
-int pow2ceil(long long v) {
-  int p = 1;
-  while (p < v) p *= 2;
-  return p;
-}
 
 // SMs of the current device (152 on GB300; also the answer when no device is visible).
 int sm_count() {
@@ -185,8 +192,6 @@ int rows_group(int TN, int C) {
     g *= 2;
   return g;
 }
-// Mid rows: chunks per 16-warp CTA.
-int mid_group(int C) { return C < 8 ? C : 8; }
 
 const tfx::KernelSet& kernels(int bits) {
   static tfx::KernelSet ks[9];
@@ -228,20 +233,25 @@ int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, v
 struct Family {
   const void* fn;
   int wpc, nr;
-  bool rows;  // the decode-rows kernel
+  bool rows;  // the decode-rows kernel; otherwise the tensor-core kernel
 };
 
 Family pick(int bits, int rows) {
   const tfx::KernelSet& ks = kernels(bits);
-  const int prow = rows < kRowsPerPass ? rows : kRowsPerPass;
   if (g_variant != 2 && rows <= 16)
-    return prow <= 8 ? Family{ks.linear_rows[0], tfx::kRowsTC * tfx::kRowsGW, 1, true}
+    return rows <= 8 ? Family{ks.linear_rows[0], tfx::kRowsTC * tfx::kRowsGW, 1, true}
                      : Family{ks.linear_rows[1], tfx::kRowsTC * tfx::kRowsGW, 2, true};
-  if (prow <= 16) return Family{ks.linear_mid[0], 16, 2, false};
-  if (prow <= 32) return Family{ks.linear_mid[1], 16, 4, false};
-  if (prow <= 64) return Family{ks.linear_mid[2], 16, 8, false};
-  return Family{ks.linear_mid[3], 16, 16, false};
+  return Family{ks.linear_tc, tfx::kTcThreads / 32, 0, false};
 }
+
+// Tensor-core kernel: chunks per CTA. All C chunks (one slab) unless the layer
+// has too few (block, pass) units to give every SM two CTAs.
+int tc_group(int NB, int passes, int C) {
+  int g = C;
+  while (g > 1 && (long long)NB * passes * (C / g) < 2LL * sm_count()) g /= 2;
+  return g;
+}
+int tc_passes(int rows) { return (rows + tfx::kTcRowsPerPass - 1) / tfx::kTcRowsPerPass; }
 
 // Opt in to more than the default 48 KB of shared memory once per kernel and size.
 int set_smem(const void* fn, size_t smem) {
@@ -288,7 +298,8 @@ int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* c
                   rows);
     sc.xf[i] = pv->xf;
     sc.partial[i] = pv->partial;
-    sc.counters[i] = pv->counters;
+    sc.counters[i] = pv->counters + tfx::kErrorInts;
+    if (i == 0) sc.err = pv->counters;
   }
   return tfx::launch_layer(ws, count, x, rows, ys, s, sc, g_pdl != 0);
 }
@@ -319,22 +330,21 @@ int chunks_of(int K) {
   return c;
 }
 
-size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows) { return (size_t)((rows + 7) / 8 * 8) * w->K * 2; }
+size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows) { return (size_t)((rows + 15) / 16 * 16) * w->K * 2; }
 
 size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
-  const int C = chunks_of(w->K), TN = w->N / 16;
-  const int p_rows = C / (rows_gw(C) * rows_group(TN, C)), p_mid = C / mid_group(C);
+  const int C = chunks_of(w->K), TN = w->N / 16, NB = w->N / 128;
+  const int p_rows = C / (rows_gw(C) * rows_group(TN, C));
+  const int p_tc = C / tc_group(NB, 1, C);  // the most slabs any pass count needs
   const int small = rows < 16 ? rows : 16;
-  size_t need = (size_t)(p_rows > p_mid ? p_rows : p_mid) * small * w->N * 4;
-  if (rows > 16) {
-    const size_t mid = (size_t)passes_of(rows) * p_mid * (rows < kRowsPerPass ? rows : kRowsPerPass) * w->N * 4;
-    if (mid > need) need = mid;
-  }
-  return need;
+  size_t need = (size_t)(p_rows > p_tc ? p_rows : p_tc) * small * w->N * 4;
+  const int rp = rows < kTcRowsPerPass ? rows : kTcRowsPerPass;
+  const size_t tc = (size_t)tc_passes(rows) * p_tc * rp * w->N * 4;
+  return tc > need ? tc : need;
 }
 
 size_t counter_bytes_needed(const tfx_exl3_weight* w, int rows) {
-  return (size_t)passes_of(rows) * (w->N / 128) * sizeof(int);
+  return (size_t)(kErrorInts + tc_passes(rows) * (w->N / 128)) * sizeof(int);
 }
 
 int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s,
@@ -346,27 +356,29 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ra.x = x;
   ra.count = count;
   ra.rows = rows;
-  ra.rows_pad = (rows + 7) / 8 * 8;
+  ra.rows_pad = (rows + 15) / 16 * 16;
   ra.K = K;
   ra.act = ws[0]->act;
   for (int i = 0; i < count; i++) {
     ra.suh[i] = reinterpret_cast<const __half*>(ws[i]->suh);
     ra.xf[i] = sc.xf[i];
   }
+  const Family f = pick(bits, rows);
+  ra.layout = f.rows ? 0 : 1;
   const long long items = (long long)ra.rows_pad * (K / 128);
   int rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
                   pdl);
   if (rc) return rc;
 
   // one grid over every member's CTAs
-  const Family f = pick(bits, rows);
   LinearArgs la = {};
   la.count = count;
   la.K = K;
   la.TK = K / 16;
   la.rows = rows;
-  la.passes = passes_of(rows);
-  la.rp = rows < kRowsPerPass ? rows : kRowsPerPass;
+  const int per_pass = f.rows ? kRowsPerPass : kTcRowsPerPass;
+  la.passes = (rows + per_pass - 1) / per_pass;
+  la.rp = rows < per_pass ? rows : per_pass;
   la.act = ws[0]->act;
   long long ctas = 0;
   for (int i = 0; i < count; i++) {
@@ -391,22 +403,27 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
       m.arrivals = (8 / kRowsTC) * m.P;
       ctas += (long long)(TN / kRowsTC) * m.P;
     } else {
-      m.G = mid_group(m.C);
-      m.TC = f.wpc / m.G > 8 ? 8 : f.wpc / m.G;
+      m.G = tc_group(m.NB, la.passes, m.C);
+      m.TC = 8;
       m.P = m.C / m.G;
-      m.arrivals = (8 / m.TC) * m.P;
-      ctas += (long long)m.NB * (8 / m.TC) * m.P * la.passes;
+      m.arrivals = m.P;
+      ctas += (long long)m.NB * m.P * la.passes;
     }
     m.log2G = __builtin_ctz(m.G);
   }
   if (ctas > 0x7fffffffLL) return fail(TFX_EUNSUPPORTED, "grid of %lld CTAs", ctas);
-  const size_t smem = f.rows ? 0 : (size_t)f.wpc * f.nr * 8 * 16 * sizeof(float);
+  const size_t smem = f.rows ? 0 : kTcDynSmem;
   rc = set_smem(f.fn, smem);
   if (rc) return rc;
+  TcArgs ta;
+  ta.la = la;
+  ta.Q = ra.rows_pad / 8;
+  ta.err = sc.err;
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && cudaEventRecord(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
-  rc = launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl);
+  rc = f.rows ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl)
+              : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
   if (rc) return rc;
   if (ea && cudaEventRecord(ea, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
   return 0;
@@ -538,6 +555,15 @@ int tfx_exl3_debug_set_driver(const tfx_exl3_driver* d) {
   }
   if (!d->alloc || !d->free || !d->memset0) return fail(TFX_EINVAL, "driver hooks must all be set");
   g_drv = *d;
+  return 0;
+}
+
+int tfx_exl3_debug_error(const tfx_exl3_weight* w, int* device_error) {
+  if (!w || !device_error) return fail(TFX_EINVAL, "null argument");
+  const Priv* pv = static_cast<const Priv*>(w->priv);
+  if (!pv || !pv->counters) return fail(TFX_ENOTRESERVED, "weight not reserved");
+  cudaError_t e = cudaMemcpy(device_error, pv->counters, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
   return 0;
 }
 

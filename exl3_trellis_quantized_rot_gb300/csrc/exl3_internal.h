@@ -14,7 +14,12 @@ struct Scratch {
   uint2* xf[3];
   float* partial[3];
   int* counters[3];
+  int* err;  // device error word (a bounded wait gave up)
 };
+
+// The counter buffer of a weight starts with this many ints: word 0 is the
+// device error word, the rest pad the counters to 16 bytes.
+constexpr int kErrorInts = 4;
 
 // K chunks of the summation order: a pure function of K.
 int chunks_of(int K);

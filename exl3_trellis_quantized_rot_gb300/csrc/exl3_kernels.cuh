@@ -77,8 +77,9 @@ struct LinearArgs {
 struct RotArgs {
   const void* x;        // rows x K, act dtype
   const __half* suh[3]; // per member
-  uint2* xf[3];         // per member output, fragment order
-  int count, rows, rows_pad, K, act;  // rows_pad = rows rounded up to 8 (padding rows are zero)
+  uint2* xf[3];         // per member output
+  int count, rows, rows_pad, K, act;  // rows_pad = rows rounded up to 16 (padding rows are zero)
+  int layout;           // 0: m16n8k16 B-fragment order (xf_index); 1: tensor-core core matrices (xc_byte)
 };
 
 struct DecodeArgs {
@@ -292,104 +293,6 @@ __device__ __forceinline__ const Member& pick_member(const LinearArgs& a) {
   if (a.count > 1 && (int)blockIdx.x >= a.m[1].cta_begin) mi = 1;
   if (a.count > 2 && (int)blockIdx.x >= a.m[2].cta_begin) mi = 2;
   return a.m[mi];
-}
-
-// ---------------------------------------------------------------------------
-// Mid-rows kernel (any row count, 128-row passes). One CTA = TC tile-columns
-// x G chunks (one warp each, WPC = TC*G) of one chunk group s of one pass.
-// The CTA folds its G chunk sums as a tree in shared memory and writes slab s.
-// NR = 8-row MMA groups per pass (rows of the pass <= 8*NR); PF = tiles of
-// trellis words prefetched per warp.
-template <int BITS, int NR, int WPC, int PF>
-__global__ void __launch_bounds__(WPC * 32, (WPC <= 8 ? 4 : 1))
-    linear_kernel(const __grid_constant__ LinearArgs a) {
-  extern __shared__ float red[];  // [WPC][NR*8][16]
-  __shared__ int s_last;
-  griddep_wait();
-  griddep_launch();
-  const Member& M = pick_member(a);
-
-  int local = blockIdx.x - M.cta_begin;
-  const int pass = local % a.passes;
-  local /= a.passes;
-  const int s = local % M.P;
-  local /= M.P;
-  const int subs = 8 / M.TC;
-  const int nb = local / subs, sub = local % subs;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int w = warp % M.G, c = warp / M.G;
-  const int tn = nb * 8 + sub * M.TC + c;
-  const int chunk = s * M.G + w;
-  const int t0 = chunk_begin(chunk, a.TK, M.C), t1 = chunk_begin(chunk + 1, a.TK, M.C);
-  const int row0 = pass * kRowsPerPass;
-  const int prow = min(kRowsPerPass, a.rows - row0);
-
-  float acc[NR][4];
-#pragma unroll
-  for (int q = 0; q < NR; q++) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-
-  if (c < M.TC) {
-    LaneWindow<BITS> lw;
-    lw.init(lane);
-    const uint32_t* tp = M.trellis + (long long)t0 * M.stride + (long long)tn * (8 * BITS);
-    const uint2* xq = M.xf + xf_index(row0 / 8, t0, lane, a.TK);
-    const long long xstride_q = 32LL * a.TK;
-    const int ntiles = t1 - t0;
-    uint32_t ring[PF][Geo<BITS>::kRaw];
-#pragma unroll
-    for (int p = 0; p < PF; p++)
-      if (p < ntiles) lw.load(tp + (long long)p * M.stride, ring[p]);
-
-    for (int it = 0; it < ntiles; it += PF) {
-#pragma unroll
-      for (int p = 0; p < PF; p++) {
-        const int tk = it + p;
-        if (tk < ntiles) {
-          uint32_t win[Geo<BITS>::kNorm + 1];
-          lw.align(ring[p], win);
-          if (tk + PF < ntiles) lw.load(tp + (long long)(tk + PF) * M.stride, ring[p]);
-          uint32_t af[4];
-          decode8<BITS>(win, af);
-#pragma unroll
-          for (int q = 0; q < NR; q++) {
-            if (8 * q < prow) {
-              const uint2 bx = __ldg(xq + q * xstride_q + 32LL * tk);
-              mma16816(acc[q], af, bx.x, bx.y);
-            }
-          }
-        }
-      }
-    }
-  }
-
-  // chunk sums -> shared memory: red[warp][r][n_local]
-  float* rw = red + warp * (NR * 8 * 16);
-#pragma unroll
-  for (int q = 0; q < NR; q++) {
-    const int r0 = 8 * q + 2 * t;
-    rw[r0 * 16 + g] = acc[q][0];
-    rw[(r0 + 1) * 16 + g] = acc[q][1];
-    rw[r0 * 16 + g + 8] = acc[q][2];
-    rw[(r0 + 1) * 16 + g + 8] = acc[q][3];
-  }
-  __syncthreads();
-
-  // tree over the CTA's G chunks -> slab s of the CTA's columns
-  const int cols = M.TC * 16;
-  const long long slab = (long long)a.rp * M.N;
-  float* part = M.partial + ((long long)pass * M.P + s) * slab;
-  for (int idx = threadIdx.x; idx < prow * cols; idx += WPC * 32) {
-    const int r = idx / cols, cc = idx - r * cols;
-    const int cw = cc >> 4, nl = cc & 15;
-    const float* src = red + (cw * M.G) * (NR * 8 * 16) + r * 16 + nl;
-    part[(long long)r * M.N + (long long)(nb * 8 + sub * M.TC) * 16 + cc] =
-        tree_load<false>(src, NR * 8 * 16, M.G);
-  }
-  if (!arrive_last(&M.counters[pass * M.NB + nb], M.arrivals, &s_last)) return;
-  block_epilogue(M, a, pass, nb, prow, row0, warp, WPC, lane);
-  __syncthreads();
-  if (threadIdx.x == 0) M.counters[pass * M.NB + nb] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -614,7 +517,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ Dec
 // Kernel pointers for one bit width (defined in exl3_bits.cu).
 struct KernelSet {
   const void* linear_rows[2];  // decode-rows family: NR = 1, 2
-  const void* linear_mid[4];   // mid-rows family: NR = 2, 4, 8, 16 (16 warps)
+  const void* linear_tc;       // tensor-core family: any row count, 64-row passes
   const void* decode;
 };
 

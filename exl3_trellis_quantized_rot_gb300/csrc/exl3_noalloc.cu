@@ -80,7 +80,8 @@ extern "C" int tfx_exl3_linear_static(const tfx_exl3_weight* w, const void* x, i
   rc = scratch_on_current_device(&base);
   if (rc) return rc;
   tfx::Scratch sc = {};
-  sc.counters[0] = reinterpret_cast<int*>(base);
+  sc.err = reinterpret_cast<int*>(base);
+  sc.counters[0] = reinterpret_cast<int*>(base) + tfx::kErrorInts;
   sc.xf[0] = reinterpret_cast<uint2*>(base + kCounterBytes);
   sc.partial[0] = reinterpret_cast<float*>(base + kCounterBytes + align256(xf_bytes));
 

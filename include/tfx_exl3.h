@@ -130,8 +130,8 @@ int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk);
 int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
 
 /* Kernel family forced for the next calls: 0 = auto (1..16 rows decode-rows,
- * more rows mid-rows), 1 = decode-rows whenever rows <= 16, 2 = mid-rows for
- * every row count. The initial value comes from TFX_EXL3_VARIANT
+ * more rows the tensor-core kernel), 1 = decode-rows whenever rows <= 16,
+ * 2 = the tensor-core kernel for every row count. The initial value comes from TFX_EXL3_VARIANT
  * (auto|rows|mid). Returns the previous value. */
 int tfx_exl3_set_variant(int variant);
 
@@ -147,6 +147,11 @@ typedef struct {
   int (*memset0)(void* p, size_t bytes, cudaStream_t s);
 } tfx_exl3_driver;
 int tfx_exl3_debug_set_driver(const tfx_exl3_driver* d);
+
+/* Device error word of a reserved weight: 1 once a tensor-core launch on it
+ * gave up a bounded wait (a broken pipeline, never expected), 0 otherwise.
+ * Synchronous copy; for tests and diagnostics. reset_counters clears it. */
+int tfx_exl3_debug_error(const tfx_exl3_weight* w, int* device_error);
 
 /* Measurement hook: the next linear/group call on this thread records
  * `before` just before its linear-kernel launch and `after` just after it,

@@ -105,7 +105,22 @@ def test_repeated_calls_need_no_memset():
         tfx.linear(w, x, y=y)
         assert same_bytes(y, first)
     assert tfx.stats(w) == (allocs, memsets) == (3, 1)
+    assert tfx.device_error(w) == 0
     assert_close(to_f64(first), oracle_y(hw, x64), what="repeat")
+
+
+def test_repeated_tensor_core_calls_need_no_memset():
+    hw, w = make(14, 5120, 1024, 4, max_rows=128)
+    x64, x = x_of(14, 100, 5120)
+    first = tfx.linear(w, x)
+    allocs, memsets = tfx.stats(w)
+    y = torch.empty_like(first)
+    for _ in range(20):
+        tfx.linear(w, x, y=y)
+        assert same_bytes(y, first)
+    assert tfx.stats(w) == (allocs, memsets)
+    assert tfx.device_error(w) == 0
+    assert_close(to_f64(first), oracle_y(hw, x64), what="tensor-core repeat")
 
 
 def test_reset_counters_then_same_bytes():

@@ -127,19 +127,19 @@ def test_reserve_grows_only_and_zeroes_counters_once_per_growth(L, drv):
     cnt_ptr = drv.memsets[0][0]
     assert drv.memsets[0][2] == stream  # on the call's stream, not the legacy stream
     assert all(a[2] == stream for a in drv.allocs)
-    # counters: 1 pass x 40 blocks
-    assert drv.memsets[0][1] == 40 * 4 and cnt_ptr in [a[0] for a in drv.allocs]
+    # counter buffer: the device error word (padded to 4 ints), then 1 pass x 40 blocks
+    assert drv.memsets[0][1] == (4 + 40) * 4 and cnt_ptr in [a[0] for a in drv.allocs]
     # same or fewer rows: nothing
     for r in (1, 7, 16):
         tfx.reserve(w, r, stream)
     assert len(drv.allocs) == 3 and len(drv.memsets) == 1
     assert tfx.stats(w) == (3, 1)
-    # more rows within one pass: scratch grows, counters do not (still 1 pass)
-    tfx.reserve(w, 100, stream)
+    # more rows within one 64-row pass: scratch grows, counters do not
+    tfx.reserve(w, 64, stream)
     assert len(drv.memsets) == 1
-    # a second pass: the counter buffer grows and is zeroed once, on the stream
+    # more passes: the counter buffer grows and is zeroed once, on the stream
     tfx.reserve(w, 200, 0x99)
-    assert len(drv.memsets) == 2 and drv.memsets[1][2] == 0x99 and drv.memsets[1][1] == 2 * 40 * 4
+    assert len(drv.memsets) == 2 and drv.memsets[1][2] == 0x99 and drv.memsets[1][1] == (4 + 4 * 40) * 4
     freed = {p for p, _ in drv.frees}
     assert cnt_ptr in freed
     tfx.release(w)
@@ -196,7 +196,7 @@ def test_reset_counters_goes_to_the_stream(L, drv):
     w = fake_weight(256, 384, 2)
     tfx.reserve(w, 4, 0x55)
     tfx.reset_counters(w, 0x66)
-    assert drv.memsets[-1][2] == 0x66 and drv.memsets[-1][1] == 3 * 4
+    assert drv.memsets[-1][2] == 0x66 and drv.memsets[-1][1] == (4 + 3) * 4
     assert tfx.stats(w) == (3, 2)
 
 
