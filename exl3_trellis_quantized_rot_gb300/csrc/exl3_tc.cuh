@@ -32,6 +32,8 @@ constexpr int kTcThreads = (kTcDecodeWarps + 1) * 32;
 constexpr int kTcSW = 24;                 // bulk-copy ring stages (one k-step each)
 constexpr int kTcXStage = kTcRowsPerPass * 32;  // x bytes per k-step: N rows x 16 k x 2 B
 constexpr int kTcAStage = 128 * 32;        // A bytes per k-step
+constexpr int kTcAB = 4;                   // A buffers (decode group g uses g, g+2)
+constexpr int kTcLag = 8;                  // a stage is refilled 8 steps after its MMA was issued
 constexpr int kTcMaxLevels = 4;            // chunk tree levels parked in TMEM (C <= 16)
 constexpr long long kTcSpin = 2000000000LL;  // clock cycles before a wait gives up
 constexpr size_t kTcDynSmem = 120 * 1024;     // >= the rings; also keeps one CTA (one TMEM allocation) per SM
@@ -49,12 +51,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(s_addr(b)) : "memory");
 }
+// try_wait may suspend the thread (here up to 0.1 ms) until the phase completes.
 __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(s_addr(b)), "r"(parity)
+      : "r"(s_addr(b)), "r"(parity), "r"(100000)
       : "memory");
   return ok != 0;
 }
@@ -145,9 +148,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   const LinearArgs& a = ta.la;
   extern __shared__ __align__(1024) unsigned char dsm[];
   unsigned char* sX = dsm;                                 // [kTcSW][kTcXStage]
-  unsigned char* sA = dsm + kTcSW * kTcXStage;             // [2][kTcAStage]
-  unsigned char* sW = sA + 2 * kTcAStage;                  // [kTcSW][8 tiles][8*BITS words]
-  __shared__ __align__(8) uint64_t full[kTcSW], slot_free[kTcSW], a_ready[2], a_free[2], chunk_done[2], fold_done[2];
+  unsigned char* sA = dsm + kTcSW * kTcXStage;             // [kTcAB][kTcAStage]
+  unsigned char* sW = sA + kTcAB * kTcAStage;              // [kTcSW][8 tiles][8*BITS words]
+  __shared__ __align__(8) uint64_t full[kTcSW], slot_free[kTcSW], a_ready[kTcAB], a_free[kTcAB], chunk_done[2],
+      fold_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_last;
@@ -179,9 +183,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
       mbar_init(&full[i], 1);
       mbar_init(&slot_free[i], 1);
     }
-    for (int i = 0; i < 2; i++) {
+    for (int i = 0; i < kTcAB; i++) {
       mbar_init(&a_ready[i], 8);
       mbar_init(&a_free[i], 1);
+    }
+    for (int i = 0; i < 2; i++) {
       mbar_init(&chunk_done[i], 1);
       mbar_init(&fold_done[i], kTcDecodeWarps);
     }
@@ -224,19 +230,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           // chunk ci reuses region cur[ci&1]: its previous user (chunk ci-2) must be folded
           if (ci >= 2 && !mbar_wait(&fold_done[ci & 1], ((ci - 2) >> 1) & 1, &s_abort, ta.err)) break;
         }
-        const int ab = i & 1, s = i % kTcSW;
-        if (!mbar_wait(&a_ready[ab], (i >> 1) & 1, &s_abort, ta.err)) break;
+        const int ab = i % kTcAB, s = i % kTcSW;
+        if (!mbar_wait(&a_ready[ab], (i / kTcAB) & 1, &s_abort, ta.err)) break;
         tc_fence_after();
         umma_f16(tmem + (uint32_t)((ci & 1) * NM), umma_desc(sA + ab * kTcAStage), umma_desc(sX + s * kTcXStage),
                  idesc, i != cfirst ? 1u : 0u);
         umma_commit(&a_free[ab]);
         umma_commit(&slot_free[s]);
         if (i + 1 == cnext) umma_commit(&chunk_done[ci & 1]);
-        // refill the stage of step i-1 once its MMA has completed (one MMA stays queued)
-        if (i >= 1 && i - 1 + kTcSW < nsteps) {
-          const int sp = (i - 1) % kTcSW;
-          if (!mbar_wait(&slot_free[sp], ((i - 1) / kTcSW) & 1, &s_abort, ta.err)) break;
-          issue(i - 1 + kTcSW);
+        // refill the stage of step i-kTcLag once its MMA has completed
+        if (i >= kTcLag && i - kTcLag + kTcSW < nsteps) {
+          const int sp = (i - kTcLag) % kTcSW;
+          if (!mbar_wait(&slot_free[sp], ((i - kTcLag) / kTcSW) & 1, &s_abort, ta.err)) break;
+          issue(i - kTcLag + kTcSW);
         }
       }
       if (s_abort) {
@@ -298,9 +304,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
       // fold finished chunks once this warp has moved past them (chunk c is done
       // when this warp decodes a step of chunk c+1)
       while (chunk_of_next_fold < cdec) fold(chunk_of_next_fold++);
-      const int s = i % kTcSW, ab = i & 1;
+      const int s = i % kTcSW, ab = i % kTcAB;
       if (!mbar_wait_warp(&full[s], (i / kTcSW) & 1, &s_abort, ta.err)) break;
-      if (i >= 2 && !mbar_wait_warp(&a_free[ab], ((i - 2) >> 1) & 1, &s_abort, ta.err)) break;
+      if (i >= kTcAB && !mbar_wait_warp(&a_free[ab], ((i - kTcAB) / kTcAB) & 1, &s_abort, ta.err)) break;
       const uint32_t* tw = reinterpret_cast<const uint32_t*>(sW + s * (8 * 32 * BITS)) + j * (8 * BITS);
       uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
       raw[0] = tw[lw.i0];
