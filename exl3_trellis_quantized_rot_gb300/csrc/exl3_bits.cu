@@ -11,8 +11,8 @@
 #define TFX_CAT(a, b) TFX_CAT2(a, b)
 
 // Launch-shape constants of the decode-rows kernel: prefetch depth and the
-// minimum resident 8-warp CTAs per SM (4 -> 64 registers, 3 -> 80) for
-// 1..8 and 9..16 rows.
+// minimum resident 8-warp CTAs per SM (4 -> 64 registers, 3 -> 80, 2 -> 128)
+// for 1..8, 9..16, 17..32 and 33..64 rows.
 #ifndef TFX_ROWS_PF1
 #define TFX_ROWS_PF1 4
 #endif
@@ -25,6 +25,18 @@
 #ifndef TFX_ROWS_MINB2
 #define TFX_ROWS_MINB2 3
 #endif
+#ifndef TFX_ROWS_PF4
+#define TFX_ROWS_PF4 2
+#endif
+#ifndef TFX_ROWS_MINB4
+#define TFX_ROWS_MINB4 ((TFX_BITS >= 5 && TFX_BITS <= 7) ? 2 : 3)
+#endif
+#ifndef TFX_ROWS_PF8
+#define TFX_ROWS_PF8 2
+#endif
+#ifndef TFX_ROWS_MINB8
+#define TFX_ROWS_MINB8 2
+#endif
 
 namespace tfx {
 
@@ -34,6 +46,10 @@ KernelSet TFX_CAT(kernels_b, TFX_BITS)() {
       reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 1, TFX_ROWS_PF1, TFX_ROWS_MINB1>);
   k.linear_rows[1] =
       reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 2, TFX_ROWS_PF2, TFX_ROWS_MINB2>);
+  k.linear_rows[2] =
+      reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 4, TFX_ROWS_PF4, TFX_ROWS_MINB4>);
+  k.linear_rows[3] =
+      reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 8, TFX_ROWS_PF8, TFX_ROWS_MINB8>);
   k.linear_tc = reinterpret_cast<const void*>(&linear_tc_kernel<TFX_BITS>);
   k.decode = reinterpret_cast<const void*>(&decode_kernel<TFX_BITS>);
   return k;

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArg
       uint2 o;
       o.x = *reinterpret_cast<uint32_t*>(&h[0]);
       o.y = *reinterpret_cast<uint32_t*>(&h[1]);
-      *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(a.xf[m]) + xc_byte(r, 128 * b + 4 * lane, a.rows_pad / 8)) = o;
+      *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(a.xf[m]) + xc_byte(r, 128 * b + 4 * lane, a.K, a.rp_tc, a.rows_pad)) = o;
     }
   }
 }
@@ -154,6 +154,9 @@ int validate(const tfx_exl3_weight* w) {
   if (w->tile_row_stride < (int64_t)(w->N / 16) * 8 * w->bits)
     return fail(TFX_EINVAL, "tile_row_stride %lld below the weight's own %lld words",
                 (long long)w->tile_row_stride, (long long)(w->N / 16) * 8 * w->bits);
+  if (w->tile_row_stride % 4)
+    return fail(TFX_EALIGN, "tile_row_stride %lld is not a multiple of 4 words (16 bytes)",
+                (long long)w->tile_row_stride);
   if (!aligned16(w->trellis) || !aligned16(w->suh) || !aligned16(w->svh))
     return fail(TFX_EALIGN, "trellis/suh/svh must be 16-byte aligned");
   return 0;
@@ -183,7 +186,8 @@ int sm_count() {
 // chunks form one CTA's subtree; G grows while the launch keeps at least
 // 4 CTAs per SM (launch shape only; the bits do not depend on it).
 int rows_gw(int C) { return C < tfx::kRowsGW ? C : tfx::kRowsGW; }
-int rows_group(int TN, int C) {
+int rows_group(int TN, int C, int rows) {
+  if (rows > 16) return 1;  // 32- and 64-row tiles park no tree levels
   const int gw = rows_gw(C);
   const long long want = 4LL * sm_count();
   int g = 1;
@@ -241,17 +245,42 @@ Family pick(int bits, int rows) {
   if (g_variant != 2 && rows <= 16)
     return rows <= 8 ? Family{ks.linear_rows[0], tfx::kRowsTC * tfx::kRowsGW, 1, true}
                      : Family{ks.linear_rows[1], tfx::kRowsTC * tfx::kRowsGW, 2, true};
+  if (g_variant != 2 && rows <= tfx::kRowsMaxRows)
+    return rows <= 32 ? Family{ks.linear_rows[2], tfx::kRowsTC * tfx::kRowsGW, 4, true}
+                      : Family{ks.linear_rows[3], tfx::kRowsTC * tfx::kRowsGW, 8, true};
   return Family{ks.linear_tc, tfx::kTcThreads / 32, 0, false};
 }
 
-// Tensor-core kernel: chunks per CTA. All C chunks (one slab) unless the layer
-// has too few (block, pass) units to give every SM two CTAs.
-int tc_group(int NB, int passes, int C) {
-  int g = C;
-  while (g > 1 && (long long)NB * passes * (C / g) < 2LL * sm_count()) g /= 2;
-  return g;
+// Tensor-core kernel: rows per pass, and chunks per work unit (G). Up to 128
+// rows run as one pass; longer calls use 64-row passes so that every unit can
+// hold all C chunks (P = 1, no slabs). Otherwise G is the power of two that
+// minimises the persistent CTAs' critical path, ceil(units / SMs) unit
+// lengths plus a fixed per-unit cost, among those whose TMEM regions fit:
+// (2 + log2 G) * rows columns <= 512. Launch shape only: the bits do not
+// depend on G.
+int tc_rows_per_pass(int rows) { return rows <= tfx::kTcRowsMax ? tfx::kTcRowsMax : tfx::kTcRowsLong; }
+int tc_passes(int rows) {
+  const int rp = tc_rows_per_pass(rows);
+  return (rows + rp - 1) / rp;
 }
-int tc_passes(int rows) { return (rows + tfx::kTcRowsPerPass - 1) / tfx::kTcRowsPerPass; }
+int tc_group(long long blocks, int rows, int C, int TK) {
+  const int passes = tc_passes(rows);
+  if (rows > tfx::kTcRowsMax) return C;
+  const int nm = (rows + 15) / 16 * 16;
+  const long long S = sm_count();
+  int best = 1;
+  long long best_cost = -1;
+  for (int g = C; g >= 1; g /= 2) {
+    if ((2 + __builtin_ctz(g)) * nm > 512) continue;
+    const long long units = blocks * passes * (C / g);
+    const long long cost = (units + S - 1) / S * ((long long)TK * g / C + 8);
+    if (best_cost < 0 || cost < best_cost) {
+      best = g;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
 
 // Opt in to more than the default 48 KB of shared memory once per kernel and size.
 int set_smem(const void* fn, size_t smem) {
@@ -333,13 +362,20 @@ int chunks_of(int K) {
 size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows) { return (size_t)((rows + 15) / 16 * 16) * w->K * 2; }
 
 size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
-  const int C = chunks_of(w->K), TN = w->N / 16, NB = w->N / 128;
-  const int p_rows = C / (rows_gw(C) * rows_group(TN, C));
-  const int p_tc = C / tc_group(NB, 1, C);  // the most slabs any pass count needs
+  const int C = chunks_of(w->K), TN = w->N / 16;
+  // decode-rows slabs: at most 16 rows with a grouping that depends on TN, or
+  // up to kRowsMaxRows rows at one chunk per warp
   const int small = rows < 16 ? rows : 16;
-  size_t need = (size_t)(p_rows > p_tc ? p_rows : p_tc) * small * w->N * 4;
-  const int rp = rows < kTcRowsPerPass ? rows : kTcRowsPerPass;
-  const size_t tc = (size_t)tc_passes(rows) * p_tc * rp * w->N * 4;
+  size_t need = (size_t)(C / (rows_gw(C) * rows_group(TN, C, small))) * small * w->N * 4;
+  if (rows > 16) {
+    const int mid = rows < kRowsMaxRows ? rows : kRowsMaxRows;
+    const size_t m = (size_t)(C / rows_gw(C)) * mid * w->N * 4;
+    need = m > need ? m : need;
+  }
+  // tensor-core slabs: one pass of at most kTcRowsMax rows, at most C slabs
+  // (calls above kTcRowsMax rows keep every chunk in one unit and write none)
+  const int rp = rows < kTcRowsMax ? rows : kTcRowsMax;
+  const size_t tc = (size_t)C * rp * w->N * 4;
   return tc > need ? tc : need;
 }
 
@@ -365,6 +401,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   }
   const Family f = pick(bits, rows);
   ra.layout = f.rows ? 0 : 1;
+  ra.rp_tc = tc_rows_per_pass(rows);
   const long long items = (long long)ra.rows_pad * (K / 128);
   int rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
                   pdl);
@@ -376,11 +413,17 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   la.K = K;
   la.TK = K / 16;
   la.rows = rows;
-  const int per_pass = f.rows ? kRowsPerPass : kTcRowsPerPass;
+  const int per_pass = f.rows ? kRowsPerPass : tc_rows_per_pass(rows);
   la.passes = (rows + per_pass - 1) / per_pass;
   la.rp = rows < per_pass ? rows : per_pass;
   la.act = ws[0]->act;
   long long ctas = 0;
+  int tcG = 0;
+  if (!f.rows) {
+    long long blocks = 0;
+    for (int i = 0; i < count; i++) blocks += ws[i]->N / 128;
+    tcG = tc_group(blocks, rows, chunks_of(K), K / 16);
+  }
   for (int i = 0; i < count; i++) {
     const tfx_exl3_weight* w = ws[i];
     Member& m = la.m[i];
@@ -397,13 +440,14 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     m.cta_begin = (int)ctas;
     if (f.rows) {
       const int TN = w->N / 16;
-      m.G = rows_group(TN, m.C);
+      m.G = rows_group(TN, m.C, rows);
       m.TC = rows_gw(m.C);  // the decode-rows kernel reads its warp-group count here
       m.P = m.C / (m.TC * m.G);
       m.arrivals = (8 / kRowsTC) * m.P;
       ctas += (long long)(TN / kRowsTC) * m.P;
     } else {
-      m.G = tc_group(m.NB, la.passes, m.C);
+      // work units (pass, block, chunk group); cta_begin holds the member's first unit
+      m.G = tcG;
       m.TC = 8;
       m.P = m.C / m.G;
       m.arrivals = m.P;
@@ -417,8 +461,14 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   if (rc) return rc;
   TcArgs ta;
   ta.la = la;
-  ta.Q = ra.rows_pad / 8;
+  ta.units = (int)ctas;
+  ta.RP = per_pass;
+  ta.NMf = per_pass < ra.rows_pad ? per_pass : ra.rows_pad;
   ta.err = sc.err;
+  if (!f.rows) {
+    const long long S = sm_count();
+    ctas = ctas < S ? ctas : S;  // persistent: one CTA per SM at most
+  }
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && cudaEventRecord(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");

@@ -80,6 +80,7 @@ struct RotArgs {
   uint2* xf[3];         // per member output
   int count, rows, rows_pad, K, act;  // rows_pad = rows rounded up to 16 (padding rows are zero)
   int layout;           // 0: m16n8k16 B-fragment order (xf_index); 1: tensor-core core matrices (xc_byte)
+  int rp_tc;            // rows per pass of layout 1
 };
 
 struct DecodeArgs {
@@ -296,7 +297,7 @@ __device__ __forceinline__ const Member& pick_member(const LinearArgs& a) {
 }
 
 // ---------------------------------------------------------------------------
-// Decode-rows kernel (1..16 rows, one pass). One CTA = WPC warps = WPC
+// Decode-rows kernel (1..64 rows in row tiles of 8*NR, one pass). One CTA = WPC warps = WPC
 // consecutive tile-columns of one 128-column block, all on the same chunk
 // group; each warp owns G consecutive chunks of its tile-column (a subtree),
 // runs their MMA chains one after the other and folds them in registers as the
@@ -405,6 +406,7 @@ __device__ __forceinline__ void rows_chain(const uint32_t* __restrict__ tp, long
 }
 
 constexpr int kRowsMaxLog2G = 3;  // up to 8 chunks per warp
+constexpr int kRowsMaxRows = 64;  // the widest decode-rows row tile (NR = 8)
 constexpr int kRowsTC = 2;        // tile-columns per decode-rows CTA
 constexpr int kRowsGW = 4;        // warp groups per tile-column (consecutive chunk groups)
 
@@ -416,14 +418,17 @@ template <int BITS, int NR, int PF, int MINB>
 __global__ void __launch_bounds__(kRowsTC * kRowsGW * 32, MINB)
     linear_rows_kernel(const __grid_constant__ LinearArgs a) {
   constexpr int WPC = kRowsTC * kRowsGW;
+  // parked tree levels: up to 2^kRowsMaxLog2G chunks per warp at 1..16 rows;
+  // wider row tiles run one chunk per warp (G = 1) and park nothing
+  constexpr int kLev = NR <= 2 ? kRowsMaxLog2G : 0;
   __shared__ int s_last;
-  __shared__ float lev[WPC][kRowsMaxLog2G][NR * 4][32];
+  __shared__ float lev[kLev ? WPC : 1][kLev ? kLev : 1][kLev ? NR * 4 : 1][32];
   __shared__ float red[kRowsTC][kRowsGW][NR * 8][16];
   griddep_wait();
   griddep_launch();
   const Member& M = pick_member(a);
 
-  // one pass (rows <= 16): blockIdx -> (column group of kRowsTC tile-columns, chunk group)
+  // one pass (rows <= 8*NR <= 64): blockIdx -> (column group of kRowsTC tile-columns, chunk group)
   const int local = blockIdx.x - M.cta_begin;
   const int gidx = local % M.P;
   const int colgrp = local / M.P;
@@ -448,18 +453,20 @@ __global__ void __launch_bounds__(kRowsTC * kRowsGW * 32, MINB)
       rows_chain<BITS, NR, PF>(col + (long long)t0 * wstride, wstride, M.xf + xf_index(0, t0, lane, a.TK),
                                xstride_q, t1 - t0, lw, lane, acc);
       // while bit l of ci is set: acc = lev[l] + acc; then park acc at the first clear bit
-      int l = 0;
-      for (; l < kRowsMaxLog2G && ((ci >> l) & 1); l++) {
+      if constexpr (kLev > 0) {
+        int l = 0;
+        for (; l < kLev && ((ci >> l) & 1); l++) {
 #pragma unroll
-        for (int q = 0; q < NR; q++)
+          for (int q = 0; q < NR; q++)
 #pragma unroll
-          for (int e = 0; e < 4; e++) acc[q][e] = lev[warp][l][q * 4 + e][lane] + acc[q][e];
-      }
-      if (ci + 1 < M.G) {
+            for (int e = 0; e < 4; e++) acc[q][e] = lev[warp][l][q * 4 + e][lane] + acc[q][e];
+        }
+        if (ci + 1 < M.G) {
 #pragma unroll
-        for (int q = 0; q < NR; q++)
+          for (int q = 0; q < NR; q++)
 #pragma unroll
-          for (int e = 0; e < 4; e++) lev[warp][l][q * 4 + e][lane] = acc[q][e];
+            for (int e = 0; e < 4; e++) lev[warp][l][q * 4 + e][lane] = acc[q][e];
+        }
       }
     }
     // warp subtree -> red[c][h]: lane (g, t) holds (n = g | g+8, r = 8q + 2t | +1)
@@ -516,8 +523,8 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ Dec
 
 // Kernel pointers for one bit width (defined in exl3_bits.cu).
 struct KernelSet {
-  const void* linear_rows[2];  // decode-rows family: NR = 1, 2
-  const void* linear_tc;       // tensor-core family: any row count, 64-row passes
+  const void* linear_rows[4];  // decode-rows family: NR = 1, 2, 4, 8 (8, 16, 32, 64 rows)
+  const void* linear_tc;       // tensor-core family: any row count, persistent
   const void* decode;
 };
 

@@ -2,7 +2,7 @@
 //
 // D[n][r] = sum_k W[k][n] * xr[r][k] per 128-column block with
 //   A = decoded weights, M = 128 output columns, K-major, in shared memory;
-//   B = rotated x rows of one 64-row pass, K-major, bulk-copied to shared memory;
+//   B = rotated x rows of one pass (up to 128 rows), K-major, bulk-copied to shared memory;
 //   D = FP32 accumulator in tensor memory (TMEM lane = output column, column = row).
 // tcgen05.mma kind::f16 with FP32 accumulation returns the same bits as the
 // m16n8k16 mma.sync chain of the decode-rows kernel for the same 16-wide k
@@ -13,12 +13,18 @@
 // row-major inside; core (row group gr, k half kh) at (2*gr + kh) * 128 bytes,
 // i.e. 128 B between k halves and 256 B between row groups.
 //
-// Roles in one CTA (17 warps): 16 decode warps in two groups (even / odd
-// k-steps, one tile per warp per step, each group owning one A buffer) and a
-// control warp whose lane 0 issues the bulk copies and, strictly in step
-// order, the MMAs. Chunk c accumulates into TMEM region cur[c&1]; once its
-// last MMA completes the decode warps fold it into the chunk tree (levels
-// parked in TMEM) while chunk c+1 accumulates. Every wait is bounded: on a
+// The kernel is persistent: one CTA per SM walks the work units
+// (member, pass, 128-column block, chunk group) in a fixed stride. The work
+// of a unit is cut into stages of kTcSK k-steps that flow through a pipeline
+// of warp roles, each synchronised by mbarriers:
+//   warps 0..15   decode: each turns 2 tiles of a stage into FP16 A operands;
+//   warps 16..19  fold: merge each finished chunk into the chunk tree (levels
+//                 parked in TMEM), then the unit's output: its slab, or the
+//                 whole rot_out epilogue when one CTA owns the block;
+//   warp 20       lane 0 issues the MMAs strictly in k order;
+//   warps 21, 22  lane 0 bulk-copies the weight words / the x rows of a stage.
+// Only one lane per warp polls a barrier, so the waits stay off the shared
+// memory pipe the MMA and copy issue also use. Every wait is bounded: on a
 // timeout the kernel records an error, stops issuing work and exits after
 // releasing TMEM.
 #pragma once
@@ -26,17 +32,33 @@
 
 namespace tfx {
 
-constexpr int kTcRowsPerPass = 64;  // rows per pass (N of the MMA, rounded up to 16)
+constexpr int kTcRowsMax = 128;   // rows per pass (MMA N) when a call has at most this many rows
+constexpr int kTcRowsLong = 64;   // rows per pass above that (keeps all C chunks in one CTA)
+constexpr int kTcSK = 4;          // k-steps per stage
 constexpr int kTcDecodeWarps = 16;
-constexpr int kTcThreads = (kTcDecodeWarps + 1) * 32;
-constexpr int kTcSW = 24;                 // bulk-copy ring stages (one k-step each)
-constexpr int kTcXStage = kTcRowsPerPass * 32;  // x bytes per k-step: N rows x 16 k x 2 B
-constexpr int kTcAStage = 128 * 32;        // A bytes per k-step
-constexpr int kTcAB = 4;                   // A buffers (decode group g uses g, g+2)
-constexpr int kTcLag = 8;                  // a stage is refilled 8 steps after its MMA was issued
-constexpr int kTcMaxLevels = 4;            // chunk tree levels parked in TMEM (C <= 16)
+constexpr int kTcFoldWarp0 = 16;  // 4 fold warps; TMEM lane quarter = warp % 4
+constexpr int kTcMmaWarp = 20;
+constexpr int kTcWWarp = 21;
+constexpr int kTcXWarp = 22;
+constexpr int kTcThreads = 23 * 32;
+constexpr int kTcXS = 4;                              // x ring stages
+constexpr int kTcXStage = kTcSK * kTcRowsMax * 32;    // x bytes per stage (16 KB)
+constexpr int kTcAB = 3;                              // A (decoded weight) buffers
+constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (16 KB)
+constexpr int kTcWBudget = 48 * 1024;                 // weight ring bytes
+constexpr int kTcExBytes = 2 * 4 * 128 * 4;           // epilogue exchange (two 4-row groups)
+constexpr int kTcMaxWS = 16;
 constexpr long long kTcSpin = 2000000000LL;  // clock cycles before a wait gives up
-constexpr size_t kTcDynSmem = 120 * 1024;     // >= the rings; also keeps one CTA (one TMEM allocation) per SM
+constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcWBudget + kTcExBytes;
+
+// Weight ring geometry for a bit width: a stage holds kTcSK tile rows of one
+// 128-column block (8 tiles of 8*BITS words each).
+template <int BITS>
+struct TcW {
+  static constexpr int kRow = 256 * BITS;  // bytes of one tile row of a block
+  static constexpr int kStage = kTcSK * kRow;
+  static constexpr int kStages = kTcWBudget / kStage < kTcMaxWS ? kTcWBudget / kStage : kTcMaxWS;
+};
 
 __device__ __forceinline__ uint32_t s_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -51,21 +73,26 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(s_addr(b)) : "memory");
 }
-// try_wait may suspend the thread (here up to 0.1 ms) until the phase completes.
 __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(s_addr(b)), "r"(parity), "r"(100000)
+      : "r"(s_addr(b)), "r"(parity)
       : "memory");
   return ok != 0;
 }
 // Wait for the phase of the given parity to complete, at most kTcSpin cycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err) {
+// A completed phase costs one try_wait; otherwise the thread polls, sleeping
+// sleep_ns between polls so that waiting warps leave the issue slots of their
+// scheduler to the warps doing work.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
+                                          int sleep_ns = 0) {
+  if (mbar_test(b, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_test(b, parity)) {
     if (*abort_flag) return false;
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (clock64() - t0 > kTcSpin) {
       *abort_flag = 1;
       atomicExch(err, 1);
@@ -73,11 +100,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile
     }
   }
   return true;
-}
-// The same wait taken by all 32 lanes of a warp, with one warp-uniform outcome.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err) {
-  const bool ok = mbar_wait(b, parity, abort_flag, err);
-  return __all_sync(0xffffffffu, ok) != 0;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -129,71 +151,158 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, const float (&v)[4]) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Rotated x in the tensor-core layout: element (r, k) at byte
-// ((tk*Q + r/8)*2 + (k%16)/8)*128 + (r%8)*16 + (k%8)*2, Q = padded rows / 8,
-// so the 64 rows of one pass at one k-step are 2 KB contiguous.
-__host__ __device__ __forceinline__ long long xc_byte(int r, int k, int Q) {
+constexpr int kTcMaxLevels = 4;  // chunk tree levels parked in TMEM (C <= 16)
+
+// Rotated x in the tensor-core layout. Rows are cut into passes of RP rows;
+// pass p holds NMp = min(RP, rows_pad - p*RP) rows (a multiple of 16) and its
+// element (r', k) sits at byte p*RP*K*2 + tk*NMp*32 + ((r'/8)*2 + (k%16)/8)*128
+// + (r'%8)*16 + (k%8)*2, so the rows of a pass at consecutive k-steps are one
+// contiguous run that a single bulk copy moves.
+__host__ __device__ __forceinline__ long long xc_byte(int r, int k, int K, int RP, int rows_pad) {
+  const int p = r / RP, rr = r - p * RP;
+  const int NMp = rows_pad - p * RP < RP ? rows_pad - p * RP : RP;
   const int tk = k >> 4, kk = k & 15;
-  return (((long long)tk * Q + (r >> 3)) * 2 + (kk >> 3)) * 128 + (r & 7) * 16 + (kk & 7) * 2;
+  return (long long)p * RP * K * 2 + (long long)tk * NMp * 32 + ((rr >> 3) * 2 + (kk >> 3)) * 128 + (rr & 7) * 16 +
+         (kk & 7) * 2;
 }
 
 struct TcArgs {
-  LinearArgs la;
-  int Q;     // padded rows / 8
-  int* err;  // device error word: set to 1 when a wait timed out
+  LinearArgs la;   // la.m[i].cta_begin is the member's first unit; la.rp the slab row stride
+  int units;       // work units of all members
+  int RP;          // rows per pass
+  int NMf;         // TMEM columns per region: min(RP, rows_pad)
+  int* err;        // device error word: set to 1 when a wait timed out
 };
+
+struct TcUnit {
+  int mi, pass, gidx, nb;
+  int tbeg, nsteps;  // first k-step and k-steps of the unit's chunks
+  int row0, prow, NMp;
+};
+
+__device__ __forceinline__ TcUnit tc_unit(const TcArgs& ta, int u) {
+  const LinearArgs& a = ta.la;
+  TcUnit U;
+  U.mi = 0;
+  if (a.count > 1 && u >= a.m[1].cta_begin) U.mi = 1;
+  if (a.count > 2 && u >= a.m[2].cta_begin) U.mi = 2;
+  const Member& M = a.m[U.mi];
+  int local = u - M.cta_begin;
+  U.gidx = local % M.P;
+  local /= M.P;
+  U.nb = local % M.NB;
+  U.pass = local / M.NB;
+  const int c0 = U.gidx * M.G;
+  U.tbeg = chunk_begin(c0, a.TK, M.C);
+  U.nsteps = chunk_begin(c0 + M.G, a.TK, M.C) - U.tbeg;
+  U.row0 = U.pass * ta.RP;
+  U.prow = min(ta.RP, a.rows - U.row0);
+  U.NMp = (U.prow + 15) & ~15;
+  return U;
+}
+
+__device__ __forceinline__ void fold_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// All 128 fold threads agree: true only if every one passed ok.
+__device__ __forceinline__ bool fold_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.cta.red.and.pred q, 1, 128, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+// One lane polls, the warp follows with a warp-uniform outcome.
+__device__ __forceinline__ bool wait_lane0(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
+                                           int lane, int sleep_ns) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(b, parity, abort_flag, err, sleep_ns);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
+// Rows r0..r0+3 of one 128-column block, thread = column n = 32*(warp%4) + lane
+// of the four fold warps: finish the Walsh-Hadamard transform over n in the
+// same stage order as fwht128 (n bits 0..4 across lanes, then bits 5 and 6
+// through shared memory), scale by 1/sqrt(128) and svh, store y.
+__device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane, float* ex, float sv, void* y,
+                                                 long long yrow0, int N, int nrows, int act) {
+#pragma unroll
+  for (int m = 0; m < 5; m++) {
+    const bool hi = (lane >> m) & 1;
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[e], 1 << m);
+      v[e] = hi ? (o - v[e]) : (v[e] + o);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; e++) ex[e * 128 + n] = v[e];
+  fold_bar();
+#pragma unroll
+  for (int e = 0; e < 4; e++) {
+    const float a5 = ex[e * 128 + (n ^ 32)], b = ex[e * 128 + (n ^ 64)], c = ex[e * 128 + (n ^ 96)];
+    const bool h5 = n & 32;
+    const float u0 = h5 ? (a5 - v[e]) : (v[e] + a5);
+    const float u1 = h5 ? (c - b) : (b + c);
+    float o = (n & 64) ? (u1 - u0) : (u0 + u1);
+    o = (o * kInvSqrt128) * sv;
+    if (e < nrows) {
+      const long long yo = yrow0 + (long long)e * N;
+      if (act == 0)
+        reinterpret_cast<__half*>(y)[yo] = __float2half_rn(o);
+      else
+        reinterpret_cast<__nv_bfloat16*>(y)[yo] = __float2bfloat16_rn(o);
+    }
+  }
+}
 
 template <int BITS>
 __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_constant__ TcArgs ta) {
+  using WG = TcW<BITS>;
+  constexpr int kWS = WG::kStages;
   const LinearArgs& a = ta.la;
   extern __shared__ __align__(1024) unsigned char dsm[];
-  unsigned char* sX = dsm;                                 // [kTcSW][kTcXStage]
-  unsigned char* sA = dsm + kTcSW * kTcXStage;             // [kTcAB][kTcAStage]
-  unsigned char* sW = sA + kTcAB * kTcAStage;              // [kTcSW][8 tiles][8*BITS words]
-  __shared__ __align__(8) uint64_t full[kTcSW], slot_free[kTcSW], a_ready[kTcAB], a_free[kTcAB], chunk_done[2],
-      fold_done[2];
+  unsigned char* sX = dsm;                                  // [kTcXS][kTcXStage]
+  unsigned char* sA = sX + kTcXS * kTcXStage;               // [kTcAB][kTcAStage]
+  unsigned char* sW = sA + kTcAB * kTcAStage;               // [kWS][WG::kStage]
+  float* sEx = reinterpret_cast<float*>(sW + kTcWBudget);   // [2][4][128]
+  __shared__ __align__(8) uint64_t wfull[kTcMaxWS], wfree[kTcMaxWS], xfull[kTcXS], xfree[kTcXS], aready[kTcAB],
+      afree[kTcAB], chunk_done[2], fold_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_last;
 
   griddep_wait();
   griddep_launch();
-  const Member& M = pick_member(a);
-  int local = blockIdx.x - M.cta_begin;
-  const int pass = local % a.passes;
-  local /= a.passes;
-  const int gidx = local % M.P;
-  const int nb = local / M.P;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = pass * kTcRowsPerPass;
-  const int prow = min(kTcRowsPerPass, a.rows - row0);
-  const int NM = (prow + 15) & ~15;  // MMA N
-  const int G = M.G;
-  const int c0 = gidx * G;  // first chunk of this CTA
-  // total steps of the CTA's chunks
-  const int tbeg = chunk_begin(c0, a.TK, M.C), tend = chunk_begin(c0 + G, a.TK, M.C);
-  const int nsteps = tend - tbeg;
-  // TMEM: two accumulator regions plus log2(G) parked tree levels, NM columns each
+  // TMEM: two accumulator regions plus log2(G) parked tree levels of NMf columns
+  int maxlog = a.m[0].log2G;
+  for (int i = 1; i < a.count; i++) maxlog = max(maxlog, a.m[i].log2G);
   uint32_t tmem_cols = 32;
-  while (tmem_cols < (uint32_t)((2 + M.log2G) * NM)) tmem_cols *= 2;
+  while (tmem_cols < (uint32_t)((2 + maxlog) * ta.NMf)) tmem_cols *= 2;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int i = 0; i < kTcSW; i++) {
-      mbar_init(&full[i], 1);
-      mbar_init(&slot_free[i], 1);
+    for (int i = 0; i < kWS; i++) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wfree[i], kTcDecodeWarps);
+    }
+    for (int i = 0; i < kTcXS; i++) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&xfree[i], 1);
     }
     for (int i = 0; i < kTcAB; i++) {
-      mbar_init(&a_ready[i], 8);
-      mbar_init(&a_free[i], 1);
+      mbar_init(&aready[i], kTcDecodeWarps);
+      mbar_init(&afree[i], 1);
     }
     for (int i = 0; i < 2; i++) {
       mbar_init(&chunk_done[i], 1);
-      mbar_init(&fold_done[i], kTcDecodeWarps);
+      mbar_init(&fold_done[i], 4);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {
+  if (warp == kTcMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s_addr(&s_tmem)),
                  "r"(tmem_cols)
                  : "memory");
@@ -203,46 +312,211 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t wbytes = 8 * 32 * BITS;        // one tile row of the block
-  const uint32_t xbytes = (uint32_t)NM * 32;     // the pass's rows at one k-step
-  const uint32_t idesc = umma_idesc(NM);
-  const unsigned char* xsrc = reinterpret_cast<const unsigned char*>(M.xf) + ((long long)(row0 >> 3) * 2) * 128;
-  const uint32_t* wsrc = M.trellis + (long long)nb * (64 * BITS);
+  const int NMf = ta.NMf;
 
-  if (warp == kTcDecodeWarps) {
-    // ---------------- control warp: bulk copies and MMAs in step order
-    if (lane == 0) {
-      auto issue = [&](int i) {
-        const int s = i % kTcSW, tk = tbeg + i;
-        mbar_expect_tx(&full[s], wbytes + xbytes);
-        bulk_g2s(sW + s * (8 * 32 * BITS), wsrc + (long long)tk * M.stride, wbytes, &full[s]);
-        bulk_g2s(sX + s * kTcXStage, xsrc + (long long)tk * ta.Q * 256, xbytes, &full[s]);
-      };
-      for (int i = 0; i < kTcSW && i < nsteps; i++) issue(i);
-      int ci = 0;                                    // current chunk (relative)
-      int cnext = chunk_begin(c0 + 1, a.TK, M.C) - tbeg;  // first step of the next chunk
-      int cfirst = 0;
-      for (int i = 0; i < nsteps && !s_abort; i++) {
-        if (i == cnext) {
-          ci++;
-          cfirst = i;
-          cnext = chunk_begin(c0 + ci + 1, a.TK, M.C) - tbeg;
-          // chunk ci reuses region cur[ci&1]: its previous user (chunk ci-2) must be folded
-          if (ci >= 2 && !mbar_wait(&fold_done[ci & 1], ((ci - 2) >> 1) & 1, &s_abort, ta.err)) break;
+  if (warp < kTcDecodeWarps) {
+    // ---------------- decode: tile column j, k-steps q0 and q0+1 of every stage
+    const int j = warp & 7, q0 = (warp >> 3) * 2;
+    LaneWindow<BITS> lw;
+    lw.init(lane);
+    const int g = lane >> 2, t = lane & 3;
+    const int off0 = 512 * j + 16 * g + 4 * t;  // A-fragment register 0 in the core-matrix layout
+    int gs = 0;
+    bool run = true;
+    for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
+      const TcUnit U = tc_unit(ta, u);
+      for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
+        const int cnt = min(kTcSK, U.nsteps - s0);
+        const int ws = gs % kWS, ab = gs % kTcAB;
+        if (!wait_lane0(&wfull[ws], (gs / kWS) & 1, &s_abort, ta.err, lane, 64)) {
+          run = false;
+          break;
         }
-        const int ab = i % kTcAB, s = i % kTcSW;
-        if (!mbar_wait(&a_ready[ab], (i / kTcAB) & 1, &s_abort, ta.err)) break;
+        uint32_t raw[2][Geo<BITS>::kRaw];
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          if (q0 + h < cnt) {
+            const uint32_t* tw =
+                reinterpret_cast<const uint32_t*>(sW + ws * WG::kStage + (q0 + h) * WG::kRow) + j * (8 * BITS);
+            raw[h][0] = tw[lw.i0];
+            raw[h][1] = tw[lw.i1];
+            if constexpr (Geo<BITS>::kRaw > 2) raw[h][2] = tw[lw.i2];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wfree[ws]);
+        if (gs >= kTcAB && !wait_lane0(&afree[ab], ((gs - kTcAB) / kTcAB) & 1, &s_abort, ta.err, lane, 64)) {
+          run = false;
+          break;
+        }
+        unsigned char* abuf = sA + ab * kTcAStage;
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          if (q0 + h < cnt) {
+            uint32_t win[Geo<BITS>::kNorm + 1], af[4];
+            lw.align(raw[h], win);
+            decode8<BITS>(win, af);
+            unsigned char* o = abuf + (q0 + h) * 4096 + off0;
+            *reinterpret_cast<uint32_t*>(o) = af[0];        // n = g,   k = 2t..
+            *reinterpret_cast<uint32_t*>(o + 256) = af[1];  // n = g+8, k = 2t..
+            *reinterpret_cast<uint32_t*>(o + 128) = af[2];  // n = g,   k = 2t+8..
+            *reinterpret_cast<uint32_t*>(o + 384) = af[3];  // n = g+8, k = 2t+8..
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aready[ab]);
+      }
+    }
+  } else if (warp < kTcFoldWarp0 + 4) {
+    // ---------------- fold and output: thread = TMEM lane = column n of the block
+    const int lg = warp & 3, n = 32 * lg + lane;
+    const uint32_t lane_base = (uint32_t)(lg * 32) << 16;
+    int gc = -1, exb = 0;
+    bool run = true;
+    for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
+      const TcUnit U = tc_unit(ta, u);
+      const Member& M = a.m[U.mi];
+      const float sv = __half2float(M.svh[U.nb * 128 + n]);
+      const long long slab = (long long)a.rp * M.N;
+      for (int c = 0; c < M.G; c++) {
+        gc++;
+        if (!fold_all(wait_lane0(&chunk_done[gc & 1], (gc >> 1) & 1, &s_abort, ta.err, lane, 128))) {
+          run = false;
+          break;
+        }
         tc_fence_after();
-        umma_f16(tmem + (uint32_t)((ci & 1) * NM), umma_desc(sA + ab * kTcAStage), umma_desc(sX + s * kTcXStage),
-                 idesc, i != cfirst ? 1u : 0u);
-        umma_commit(&a_free[ab]);
-        umma_commit(&slot_free[s]);
-        if (i + 1 == cnext) umma_commit(&chunk_done[ci & 1]);
-        // refill the stage of step i-kTcLag once its MMA has completed
-        if (i >= kTcLag && i - kTcLag + kTcSW < nsteps) {
-          const int sp = (i - kTcLag) % kTcSW;
-          if (!mbar_wait(&slot_free[sp], ((i - kTcLag) / kTcSW) & 1, &s_abort, ta.err)) break;
-          issue(i - kTcLag + kTcSW);
+        const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * NMf);
+        const bool final = c + 1 == M.G;
+        for (int cc = 0; cc < U.NMp; cc += 4) {
+          float v[4];
+          tmem_ld4(cur + (uint32_t)cc, v);
+          int l = 0;
+          for (; l < kTcMaxLevels && ((c >> l) & 1); l++) {
+            float w4[4];
+            tmem_ld4(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), w4);
+#pragma unroll
+            for (int e = 0; e < 4; e++) v[e] = w4[e] + v[e];
+          }
+          if (!final) {
+            tmem_st4(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), v);
+          } else if (M.P == 1) {
+            tc_rot_out_store(v, n, lane, sEx + (exb & 1) * 512, sv, M.y,
+                             (long long)(U.row0 + cc) * M.N + U.nb * 128 + n, M.N, U.prow - cc, a.act);
+            exb++;
+          } else {
+            float* part = M.partial + ((long long)U.pass * M.P + U.gidx) * slab + (long long)cc * M.N + U.nb * 128 + n;
+#pragma unroll
+            for (int e = 0; e < 4; e++)
+              if (cc + e < U.prow) part[(long long)e * M.N] = v[e];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&fold_done[gc & 1]);
+      }
+      if (!run) break;
+      if (M.P > 1) {
+        // publish the slab; the last of the block's P units folds the slabs and rotates back
+        fold_bar();
+        if (warp == kTcFoldWarp0 && lane == 0) {
+          __threadfence();
+          const int old = atomicAdd(&M.counters[U.pass * M.NB + U.nb], 1);
+          const bool last = old == M.arrivals - 1;
+          if (last) __threadfence();
+          s_last = last;
+        }
+        fold_bar();
+        if (s_last) {
+          const float* base = M.partial + (long long)U.pass * M.P * slab + U.nb * 128 + n;
+          for (int cc = 0; cc < U.prow; cc += 4) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++)
+              v[e] = cc + e < U.prow ? tree_load<true>(base + (long long)(cc + e) * M.N, slab, M.P) : 0.f;
+            tc_rot_out_store(v, n, lane, sEx + (exb & 1) * 512, sv, M.y,
+                             (long long)(U.row0 + cc) * M.N + U.nb * 128 + n, M.N, U.prow - cc, a.act);
+            exb++;
+          }
+          if (warp == kTcFoldWarp0 && lane == 0) M.counters[U.pass * M.NB + U.nb] = 0;
+        }
+        fold_bar();
+      }
+    }
+  } else if (warp == kTcMmaWarp) {
+    // ---------------- MMA issue, strictly in k order
+    if (lane == 0) {
+      // descriptors advance by (byte offset >> 4) within the 256 KB shared window
+      const uint64_t da0 = umma_desc(sA), db0 = umma_desc(sX);
+      int gs = 0, gc = -1;
+      bool run = true;
+      for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
+        const TcUnit U = tc_unit(ta, u);
+        const Member& M = a.m[U.mi];
+        const uint32_t idesc = umma_idesc(U.NMp);
+        const int log2C = __ffs(M.C) - 1;
+        const int c0 = U.gidx * M.G;
+        int ci = -1, cnext = 0;
+        uint32_t acc = 0, dcol = 0;
+        for (int s0 = 0; run && s0 < U.nsteps; s0 += kTcSK, gs++) {
+          const int cnt = min(kTcSK, U.nsteps - s0);
+          const int ab = gs % kTcAB, xs = gs % kTcXS;
+          if (!mbar_wait(&aready[ab], (gs / kTcAB) & 1, &s_abort, ta.err) ||
+              !mbar_wait(&xfull[xs], (gs / kTcXS) & 1, &s_abort, ta.err)) {
+            run = false;
+            break;
+          }
+          tc_fence_after();
+          uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
+          uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
+          const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
+          for (int q = 0; q < cnt; q++) {
+            const int i = s0 + q;
+            if (i == cnext) {
+              ci++;
+              gc++;
+              acc = 0;
+              dcol = (uint32_t)((gc & 1) * NMf);
+              cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
+              // the region of chunk gc last held chunk gc-2: it must have been folded
+              if (gc >= 2 && !mbar_wait(&fold_done[gc & 1], ((gc - 2) >> 1) & 1, &s_abort, ta.err)) {
+                run = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            umma_f16(tmem + dcol, da, db, idesc, acc);
+            acc = 1;
+            if (i + 1 == cnext) umma_commit(&chunk_done[gc & 1]);
+            da += 4096 >> 4;
+            db += db_step;
+          }
+          if (!run) break;
+          umma_commit(&afree[ab]);
+          umma_commit(&xfree[xs]);
+        }
+      }
+    }
+  } else if (warp == kTcWWarp) {
+    // ---------------- weight words: kTcSK tile rows of the block per stage
+    if (lane == 0) {
+      int gs = 0;
+      bool run = true;
+      for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
+        const TcUnit U = tc_unit(ta, u);
+        const Member& M = a.m[U.mi];
+        const uint32_t* wsrc = M.trellis + (long long)U.nb * (64 * BITS);
+        for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
+          const int cnt = min(kTcSK, U.nsteps - s0);
+          const int ws = gs % kWS;
+          if (gs >= kWS && !mbar_wait(&wfree[ws], ((gs - kWS) / kWS) & 1, &s_abort, ta.err, 32)) {
+            run = false;
+            break;
+          }
+          mbar_expect_tx(&wfull[ws], (uint32_t)(cnt * WG::kRow));
+          for (int q = 0; q < cnt; q++)
+            bulk_g2s(sW + ws * WG::kStage + q * WG::kRow, wsrc + (long long)(U.tbeg + s0 + q) * M.stride, WG::kRow,
+                     &wfull[ws]);
         }
       }
       if (s_abort) {
@@ -253,98 +527,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
       }
     }
   } else {
-    // ---------------- decode warps
-    const int dg = warp >> 3, j = warp & 7;  // group, tile-column within the block
-    LaneWindow<BITS> lw;
-    lw.init(lane);
-    const int g = lane >> 2, t = lane & 3;
-    // A-fragment register m of tile j -> byte offset of its 4-byte pair in the core-matrix layout
-    const int off0 = 512 * j + 16 * g + 4 * t;
-    const int lg = warp & 3, cq = warp >> 2;  // TMEM lane group, column quarter (for the fold)
-    const int qcols = NM >> 2;                // columns per warp in the fold
-    float res[16];                            // this warp's share of the CTA's subtree after the last fold
-    int chunk_of_next_fold = 0;
-    int cnext_dec = chunk_begin(c0 + 1, a.TK, M.C) - tbeg;
-    int cdec = 0;  // chunk of the step being decoded
-
-    // fold of chunk cf (relative): merge cur[cf&1] into the tree levels
-    auto fold = [&](int cf) {
-      if (!mbar_wait_warp(&chunk_done[cf & 1], (cf >> 1) & 1, &s_abort, ta.err)) return;
-      tc_fence_after();
-      const uint32_t lane_base = (uint32_t)(lg * 32) << 16;
-      for (int cc = 0; cc < qcols; cc += 4) {
-        const uint32_t col = (uint32_t)(cq * qcols + cc);
-        float v[4];
-        tmem_ld4(tmem + lane_base + (uint32_t)((cf & 1) * NM) + col, v);
-        int l = 0;
-        for (; l < kTcMaxLevels && ((cf >> l) & 1); l++) {
-          float u[4];
-          tmem_ld4(tmem + lane_base + (uint32_t)((2 + l) * NM) + col, u);
-#pragma unroll
-          for (int e = 0; e < 4; e++) v[e] = u[e] + v[e];
-        }
-        if (cf + 1 < G) {
-          tmem_st4(tmem + lane_base + (uint32_t)((2 + l) * NM) + col, v);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; e++) res[cc + e] = v[e];
+    // ---------------- x rows of the pass: one contiguous run per stage
+    if (lane == 0) {
+      int gs = 0;
+      bool run = true;
+      for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
+        const TcUnit U = tc_unit(ta, u);
+        const Member& M = a.m[U.mi];
+        const unsigned char* xsrc =
+            reinterpret_cast<const unsigned char*>(M.xf) + (long long)U.pass * ta.RP * a.K * 2;
+        for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
+          const int cnt = min(kTcSK, U.nsteps - s0);
+          const int xs = gs % kTcXS;
+          if (gs >= kTcXS && !mbar_wait(&xfree[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, 32)) {
+            run = false;
+            break;
+          }
+          const uint32_t bytes = (uint32_t)(cnt * U.NMp * 32);
+          mbar_expect_tx(&xfull[xs], bytes);
+          bulk_g2s(sX + xs * kTcXStage, xsrc + (long long)(U.tbeg + s0) * U.NMp * 32, bytes, &xfull[xs]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&fold_done[cf & 1]);
-    };
-
-    for (int i = dg; i < nsteps; i += 2) {
-      if (__any_sync(0xffffffffu, s_abort)) break;
-      while (i >= cnext_dec) {
-        cdec++;
-        cnext_dec = chunk_begin(c0 + cdec + 1, a.TK, M.C) - tbeg;
-      }
-      // fold finished chunks once this warp has moved past them (chunk c is done
-      // when this warp decodes a step of chunk c+1)
-      while (chunk_of_next_fold < cdec) fold(chunk_of_next_fold++);
-      const int s = i % kTcSW, ab = i % kTcAB;
-      if (!mbar_wait_warp(&full[s], (i / kTcSW) & 1, &s_abort, ta.err)) break;
-      if (i >= kTcAB && !mbar_wait_warp(&a_free[ab], ((i - kTcAB) / kTcAB) & 1, &s_abort, ta.err)) break;
-      const uint32_t* tw = reinterpret_cast<const uint32_t*>(sW + s * (8 * 32 * BITS)) + j * (8 * BITS);
-      uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
-      raw[0] = tw[lw.i0];
-      raw[1] = tw[lw.i1];
-      if constexpr (Geo<BITS>::kRaw > 2) raw[2] = tw[lw.i2];
-      lw.align(raw, win);
-      decode8<BITS>(win, af);
-      unsigned char* abuf = sA + ab * kTcAStage;
-      *reinterpret_cast<uint32_t*>(abuf + off0) = af[0];        // n = g,   k = 2t..
-      *reinterpret_cast<uint32_t*>(abuf + off0 + 256) = af[1];  // n = g+8, k = 2t..
-      *reinterpret_cast<uint32_t*>(abuf + off0 + 128) = af[2];  // n = g,   k = 2t+8..
-      *reinterpret_cast<uint32_t*>(abuf + off0 + 384) = af[3];  // n = g+8, k = 2t+8..
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&a_ready[ab]);
-    }
-    while (!__any_sync(0xffffffffu, s_abort) && chunk_of_next_fold < G) fold(chunk_of_next_fold++);
-
-    // subtree sum -> slab gidx: TMEM lane = column 32*lg + lane, columns = rows
-    if (!__any_sync(0xffffffffu, s_abort)) {
-      float* part = M.partial + ((long long)pass * M.P + gidx) * a.rp * M.N + nb * 128 + lg * 32 + lane;
-      for (int cc = 0; cc < qcols; cc++) {
-        const int r = cq * qcols + cc;
-        if (r < prow) part[(long long)r * M.N] = res[cc];
+      if (s_abort) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 2000000) {
+        }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kTcMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
   }
-  if (s_abort) return;
-  if (!arrive_last(&M.counters[pass * M.NB + nb], M.arrivals, &s_last)) return;
-  block_epilogue(M, a, pass, nb, prow, row0, warp, kTcDecodeWarps + 1, lane);
-  __syncthreads();
-  if (threadIdx.x == 0) M.counters[pass * M.NB + nb] = 0;
 }
 
 }  // namespace tfx

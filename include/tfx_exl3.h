@@ -35,7 +35,7 @@ extern "C" {
 #define TFX_EINVAL -1        /* bad argument: shape, bits, count, null pointer */
 #define TFX_ENOTRESERVED -2  /* rows above the reserved capacity, or no reserve() yet */
 #define TFX_EUNSUPPORTED -3  /* valid but not served (e.g. group members of unequal K) */
-#define TFX_EALIGN -4        /* a pointer is not 16-byte aligned */
+#define TFX_EALIGN -4        /* a pointer (or the tile-row stride) is not 16-byte aligned */
 #define TFX_ECUDA -5         /* a CUDA runtime call failed; see tfx_exl3_last_error() */
 
 typedef enum { TFX_F16 = 0, TFX_BF16 = 1 } tfx_dtype;
@@ -48,7 +48,8 @@ typedef enum { TFX_F16 = 0, TFX_BF16 = 1 } tfx_dtype;
  * svh     : N FP16 values (the output sign flips / scales).
  * K, N    : multiples of 128. bits: 1..8.
  * tile_row_stride : words between tile rows; (N/16)*8*bits for a full weight,
- *           the parent's value for a column view.
+ *           the parent's value for a column view. A multiple of 4 words
+ *           (TFX_EALIGN otherwise): tile rows are copied as 16-byte runs.
  * act     : dtype of x and y.
  * priv    : library-owned state (scratch, counters), NULL until reserve(). */
 typedef struct {
@@ -65,8 +66,9 @@ typedef struct {
  * rows == 0 is a no-op. rows above the reserved max_rows -> TFX_ENOTRESERVED.
  * Enqueued on `stream`; allocates nothing and clears nothing (the counters
  * are reset by the kernel itself). Calls on one weight must be ordered on
- * one stream. Rows are cut into 128-row passes (PR #1475, "What this changes":
- * counters indexed pass*NB + nb). */
+ * one stream. Rows are cut into passes (PR #1475, "What this changes":
+ * counters indexed pass*NB + nb): one pass up to 128 rows, 64-row passes
+ * above that. */
 int tfx_exl3_linear(tfx_exl3_weight* w, const void* x, int rows, void* y, cudaStream_t stream);
 
 /* One rotation launch and one linear launch for up to 3 weights of the same
