@@ -85,6 +85,49 @@ __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArg
   }
 }
 
+__global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ CombineArgs ca) {
+  griddep_wait();
+  griddep_launch();
+  const LinearArgs& a = ca.la;
+  long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  int mi = 0;
+  while (mi < a.count && w >= ca.items[mi]) {
+    w -= ca.items[mi];
+    mi++;
+  }
+  if (mi >= a.count) return;
+  const Member& M = a.m[mi];
+  if (M.P <= 1) return;
+  const int r = (int)(w / M.NB), nb = (int)(w % M.NB);  // r: row of the call
+  const int pass = r / ca.RP, rr = r - pass * ca.RP;
+  const int n0 = nb * 128 + 4 * lane;
+  const long long slab = (long long)a.rp * M.N;
+  const float* base = M.partial + (long long)pass * M.P * slab + (long long)rr * M.N + n0;
+  float v[4];
+#pragma unroll
+  for (int e = 0; e < 4; e++) v[e] = tree_load<true>(base + e, slab, M.P);
+  fwht128(v, lane);
+  float sv[4];
+#pragma unroll
+  for (int e = 0; e < 4; e++) sv[e] = __half2float(M.svh[n0 + e]);
+#pragma unroll
+  for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
+  const long long yo = (long long)r * M.N + n0;
+  uint2 out;
+  if (a.act == 0) {
+    __half2 o0 = __floats2half2_rn(v[0], v[1]), o1 = __floats2half2_rn(v[2], v[3]);
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(M.y) + yo) = out;
+  } else {
+    __nv_bfloat162 o0 = __floats2bfloat162_rn(v[0], v[1]), o1 = __floats2bfloat162_rn(v[2], v[3]);
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(M.y) + yo) = out;
+  }
+}
+
 }  // namespace tfx
 
 namespace {
@@ -475,6 +518,22 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   rc = f.rows ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl)
               : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
   if (rc) return rc;
+  if (!f.rows) {
+    // members split over P > 1 units: fold their slabs, one warp per (row, block)
+    CombineArgs ca = {};
+    ca.la = la;
+    ca.RP = per_pass;
+    long long warps = 0;
+    for (int i = 0; i < count; i++) {
+      ca.items[i] = la.m[i].P > 1 ? (long long)rows * la.m[i].NB : 0;
+      warps += ca.items[i];
+    }
+    if (warps > 0) {
+      rc = launch(reinterpret_cast<const void*>(&tc_combine_kernel), dim3((unsigned)((warps + 7) / 8)), dim3(256), 0,
+                  s, &ca, pdl);
+      if (rc) return rc;
+    }
+  }
   if (ea && cudaEventRecord(ea, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
   return 0;
 }

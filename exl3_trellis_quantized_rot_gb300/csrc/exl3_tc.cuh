@@ -15,18 +15,21 @@
 //
 // The kernel is persistent: one CTA per SM walks the work units
 // (member, pass, 128-column block, chunk group) in a fixed stride. The work
-// of a unit is cut into stages of kTcSK k-steps that flow through a pipeline
-// of warp roles, each synchronised by mbarriers:
-//   warps 0..15   decode: each turns 2 tiles of a stage into FP16 A operands;
+// of a unit is cut into stages of kTcSK k-steps that flow through warp roles:
+//   warps 0..15   decode: load their tiles' words straight from global memory
+//                 one stage ahead and turn 4 tiles per stage into FP16 A operands;
 //   warps 16..19  fold: merge each finished chunk into the chunk tree (levels
-//                 parked in TMEM), then the unit's output: its slab, or the
-//                 whole rot_out epilogue when one CTA owns the block;
-//   warp 20       lane 0 issues the MMAs strictly in k order;
-//   warps 21, 22  lane 0 bulk-copies the weight words / the x rows of a stage.
-// Only one lane per warp polls a barrier, so the waits stay off the shared
-// memory pipe the MMA and copy issue also use. Every wait is bounded: on a
-// timeout the kernel records an error, stops issuing work and exits after
-// releasing TMEM.
+//                 parked in TMEM), then write the unit's output: the whole
+//                 rot_out epilogue when one unit covers all C chunks, else its
+//                 FP32 slab, which tc_combine_kernel folds afterwards;
+//   warp 20       issues the MMAs strictly in k order (lane 0);
+//   warp 21       bulk-copies the x rows of each stage (lane 0).
+// Hand-offs between the decode warps, the MMA warp and the fold warps use
+// hardware named barriers (waiting warps are descheduled, nothing polls);
+// completions of the asynchronous units (bulk copies, MMAs) are mbarriers that
+// one lane polls. Every mbarrier wait is bounded: on a timeout the kernel
+// records an error and from then on skips all work while still taking every
+// named barrier, so each warp reaches the end and TMEM is released.
 #pragma once
 #include "exl3_kernels.cuh"
 
@@ -34,31 +37,26 @@ namespace tfx {
 
 constexpr int kTcRowsMax = 128;   // rows per pass (MMA N) when a call has at most this many rows
 constexpr int kTcRowsLong = 64;   // rows per pass above that (keeps all C chunks in one CTA)
-constexpr int kTcSK = 4;          // k-steps per stage
+constexpr int kTcSK = 8;          // k-steps per stage
 constexpr int kTcDecodeWarps = 16;
 constexpr int kTcFoldWarp0 = 16;  // 4 fold warps; TMEM lane quarter = warp % 4
 constexpr int kTcMmaWarp = 20;
-constexpr int kTcWWarp = 21;
-constexpr int kTcXWarp = 22;
-constexpr int kTcThreads = 23 * 32;
-constexpr int kTcXS = 4;                              // x ring stages
-constexpr int kTcXStage = kTcSK * kTcRowsMax * 32;    // x bytes per stage (16 KB)
+constexpr int kTcXWarp = 21;
+constexpr int kTcThreads = 22 * 32;
+constexpr int kTcXS = 3;                              // x ring stages
+constexpr int kTcXStage = kTcSK * kTcRowsMax * 32;    // x bytes per stage (32 KB)
 constexpr int kTcAB = 3;                              // A (decoded weight) buffers
-constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (16 KB)
-constexpr int kTcWBudget = 48 * 1024;                 // weight ring bytes
+constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (32 KB)
 constexpr int kTcExBytes = 2 * 4 * 128 * 4;           // epilogue exchange (two 4-row groups)
-constexpr int kTcMaxWS = 16;
 constexpr long long kTcSpin = 2000000000LL;  // clock cycles before a wait gives up
-constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcWBudget + kTcExBytes;
-
-// Weight ring geometry for a bit width: a stage holds kTcSK tile rows of one
-// 128-column block (8 tiles of 8*BITS words each).
-template <int BITS>
-struct TcW {
-  static constexpr int kRow = 256 * BITS;  // bytes of one tile row of a block
-  static constexpr int kStage = kTcSK * kRow;
-  static constexpr int kStages = kTcWBudget / kStage < kTcMaxWS ? kTcWBudget / kStage : kTcMaxWS;
-};
+constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcExBytes;
+// named barriers (0 is __syncthreads)
+constexpr int kBarFold = 1;        // the 4 fold warps
+constexpr int kBarReady = 2;       // + A buffer: decode warps -> MMA warp (3 ids)
+constexpr int kBarFree = 5;        // + A buffer: MMA warp -> decode warps (3 ids)
+constexpr int kBarFolded = 8;      // + chunk parity: fold warps -> MMA warp (2 ids)
+constexpr int kReadyThreads = (kTcDecodeWarps + 1) * 32;
+constexpr int kFoldedThreads = 5 * 32;
 
 __device__ __forceinline__ uint32_t s_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -88,6 +86,7 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
 // scheduler to the warps doing work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
                                           int sleep_ns = 0) {
+  if (*abort_flag) return false;
   if (mbar_test(b, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_test(b, parity)) {
@@ -153,6 +152,11 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, const float (&v)[4]) {
 
 constexpr int kTcMaxLevels = 4;  // chunk tree levels parked in TMEM (C <= 16)
 
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Rotated x in the tensor-core layout. Rows are cut into passes of RP rows;
 // pass p holds NMp = min(RP, rows_pad - p*RP) rows (a multiple of 16) and its
 // element (r', k) sits at byte p*RP*K*2 + tk*NMp*32 + ((r'/8)*2 + (k%16)/8)*128
@@ -171,7 +175,7 @@ struct TcArgs {
   int units;       // work units of all members
   int RP;          // rows per pass
   int NMf;         // TMEM columns per region: min(RP, rows_pad)
-  int* err;        // device error word: set to 1 when a wait timed out
+  int* err;        // device error word: 1 when a wait timed out, 2 on a short shared-memory launch
 };
 
 struct TcUnit {
@@ -201,7 +205,7 @@ __device__ __forceinline__ TcUnit tc_unit(const TcArgs& ta, int u) {
   return U;
 }
 
-__device__ __forceinline__ void fold_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void fold_bar() { bar_sync(kBarFold, 128); }
 // All 128 fold threads agree: true only if every one passed ok.
 __device__ __forceinline__ bool fold_all(bool ok) {
   uint32_t r;
@@ -257,24 +261,37 @@ __device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane,
   }
 }
 
+// Stages of this CTA's units (the same count in every role).
+__device__ __forceinline__ int tc_stages_of_cta(const TcArgs& ta) {
+  int n = 0;
+  for (int u = blockIdx.x; u < ta.units; u += gridDim.x) n += (tc_unit(ta, u).nsteps + kTcSK - 1) / kTcSK;
+  return n;
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_constant__ TcArgs ta) {
-  using WG = TcW<BITS>;
-  constexpr int kWS = WG::kStages;
+  using WF = WordFetch<BITS>;
+  constexpr int kH = kTcSK / 2;  // tiles per decode warp per stage
   const LinearArgs& a = ta.la;
   extern __shared__ __align__(1024) unsigned char dsm[];
   unsigned char* sX = dsm;                                  // [kTcXS][kTcXStage]
   unsigned char* sA = sX + kTcXS * kTcXStage;               // [kTcAB][kTcAStage]
-  unsigned char* sW = sA + kTcAB * kTcAStage;               // [kWS][WG::kStage]
-  float* sEx = reinterpret_cast<float*>(sW + kTcWBudget);   // [2][4][128]
-  __shared__ __align__(8) uint64_t wfull[kTcMaxWS], wfree[kTcMaxWS], xfull[kTcXS], xfree[kTcXS], aready[kTcAB],
-      afree[kTcAB], chunk_done[2], fold_done[2];
+  float* sEx = reinterpret_cast<float*>(sA + kTcAB * kTcAStage);  // [2][4][128]
+  __shared__ __align__(8) uint64_t xfull[kTcXS], xfree[kTcXS], amma[kTcAB], chunk_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_last;
 
   griddep_wait();
   griddep_launch();
+  {
+    // the launch must provide the shared memory this build lays out
+    uint32_t dyn;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (dyn < kTcDynSmem) {
+      if (threadIdx.x == 0) atomicExch(ta.err, 2);
+      return;
+    }
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // TMEM: two accumulator regions plus log2(G) parked tree levels of NMf columns
   int maxlog = a.m[0].log2G;
@@ -284,22 +301,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int i = 0; i < kWS; i++) {
-      mbar_init(&wfull[i], 1);
-      mbar_init(&wfree[i], kTcDecodeWarps);
-    }
     for (int i = 0; i < kTcXS; i++) {
       mbar_init(&xfull[i], 1);
       mbar_init(&xfree[i], 1);
     }
-    for (int i = 0; i < kTcAB; i++) {
-      mbar_init(&aready[i], kTcDecodeWarps);
-      mbar_init(&afree[i], 1);
-    }
-    for (int i = 0; i < 2; i++) {
-      mbar_init(&chunk_done[i], 1);
-      mbar_init(&fold_done[i], 4);
-    }
+    for (int i = 0; i < kTcAB; i++) mbar_init(&amma[i], 1);
+    for (int i = 0; i < 2; i++) mbar_init(&chunk_done[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kTcMmaWarp) {
@@ -315,46 +322,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   const int NMf = ta.NMf;
 
   if (warp < kTcDecodeWarps) {
-    // ---------------- decode: tile column j, k-steps q0 and q0+1 of every stage
-    const int j = warp & 7, q0 = (warp >> 3) * 2;
+    // ---------------- decode: tile column j, k-steps q0 .. q0+kH-1 of every stage
+    const int j = warp & 7, q0 = (warp >> 3) * kH;
     LaneWindow<BITS> lw;
     lw.init(lane);
     const int g = lane >> 2, t = lane & 3;
     const int off0 = 512 * j + 16 * g + 4 * t;  // A-fragment register 0 in the core-matrix layout
-    int gs = 0;
-    bool run = true;
-    for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
-      const TcUnit U = tc_unit(ta, u);
-      for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
-        const int cnt = min(kTcSK, U.nsteps - s0);
-        const int ws = gs % kWS, ab = gs % kTcAB;
-        if (!wait_lane0(&wfull[ws], (gs / kWS) & 1, &s_abort, ta.err, lane, 64)) {
-          run = false;
-          break;
-        }
-        uint32_t raw[2][Geo<BITS>::kRaw];
+    // words of the next stage, loaded one stage ahead
+    uint32_t own[kH][WF::kOwn];
+    auto load_stage = [&](const TcUnit& U, int s0) {
+      const Member& M = a.m[U.mi];
+      const uint32_t* col = M.trellis + (long long)(U.nb * 8 + j) * (8 * BITS);
 #pragma unroll
-        for (int h = 0; h < 2; h++) {
-          if (q0 + h < cnt) {
-            const uint32_t* tw =
-                reinterpret_cast<const uint32_t*>(sW + ws * WG::kStage + (q0 + h) * WG::kRow) + j * (8 * BITS);
-            raw[h][0] = tw[lw.i0];
-            raw[h][1] = tw[lw.i1];
-            if constexpr (Geo<BITS>::kRaw > 2) raw[h][2] = tw[lw.i2];
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&wfree[ws]);
-        if (gs >= kTcAB && !wait_lane0(&afree[ab], ((gs - kTcAB) / kTcAB) & 1, &s_abort, ta.err, lane, 64)) {
-          run = false;
-          break;
-        }
+      for (int h = 0; h < kH; h++)
+        if (s0 + q0 + h < U.nsteps) WF::load(col + (long long)(U.tbeg + s0 + q0 + h) * M.stride, lw, lane, own[h]);
+    };
+    int u = blockIdx.x, s0 = 0, gs = 0;
+    TcUnit U;
+    if (u < ta.units) {
+      U = tc_unit(ta, u);
+      load_stage(U, 0);
+    }
+    while (u < ta.units) {
+      const int cnt = min(kTcSK, U.nsteps - s0);
+      uint32_t cur[kH][WF::kOwn];
+#pragma unroll
+      for (int h = 0; h < kH; h++)
+#pragma unroll
+        for (int i = 0; i < WF::kOwn; i++) cur[h][i] = own[h][i];
+      // advance and prefetch the next stage's words (possibly of the next unit)
+      int u1 = u, s1 = s0 + kTcSK;
+      TcUnit U1 = U;
+      if (s1 >= U.nsteps) {
+        u1 = u + gridDim.x;
+        s1 = 0;
+        if (u1 < ta.units) U1 = tc_unit(ta, u1);
+      }
+      if (u1 < ta.units) load_stage(U1, s1);
+      const int ab = gs % kTcAB;
+      if (gs >= kTcAB) bar_sync(kBarFree + ab, kReadyThreads);
+      if (!s_abort) {
         unsigned char* abuf = sA + ab * kTcAStage;
 #pragma unroll
-        for (int h = 0; h < 2; h++) {
+        for (int h = 0; h < kH; h++) {
           if (q0 + h < cnt) {
-            uint32_t win[Geo<BITS>::kNorm + 1], af[4];
-            lw.align(raw[h], win);
+            uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
+            WF::gather(cur[h], lw, lane, raw);
+            lw.align(raw, win);
             decode8<BITS>(win, af);
             unsigned char* o = abuf + (q0 + h) * 4096 + off0;
             *reinterpret_cast<uint32_t*>(o) = af[0];        // n = g,   k = 2t..
@@ -364,159 +378,139 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           }
         }
         fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&aready[ab]);
       }
+      bar_arrive(kBarReady + ab, kReadyThreads);
+      gs++;
+      u = u1;
+      s0 = s1;
+      U = U1;
     }
   } else if (warp < kTcFoldWarp0 + 4) {
     // ---------------- fold and output: thread = TMEM lane = column n of the block
     const int lg = warp & 3, n = 32 * lg + lane;
     const uint32_t lane_base = (uint32_t)(lg * 32) << 16;
     int gc = -1, exb = 0;
-    bool run = true;
-    for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
+    for (int u = blockIdx.x; u < ta.units; u += gridDim.x) {
       const TcUnit U = tc_unit(ta, u);
       const Member& M = a.m[U.mi];
       const float sv = __half2float(M.svh[U.nb * 128 + n]);
       const long long slab = (long long)a.rp * M.N;
       for (int c = 0; c < M.G; c++) {
         gc++;
-        if (!fold_all(wait_lane0(&chunk_done[gc & 1], (gc >> 1) & 1, &s_abort, ta.err, lane, 128))) {
-          run = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * NMf);
-        const bool final = c + 1 == M.G;
-        for (int cc = 0; cc < U.NMp; cc += 4) {
-          float v[4];
-          tmem_ld4(cur + (uint32_t)cc, v);
-          int l = 0;
-          for (; l < kTcMaxLevels && ((c >> l) & 1); l++) {
-            float w4[4];
-            tmem_ld4(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), w4);
-#pragma unroll
-            for (int e = 0; e < 4; e++) v[e] = w4[e] + v[e];
-          }
-          if (!final) {
-            tmem_st4(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), v);
-          } else if (M.P == 1) {
-            tc_rot_out_store(v, n, lane, sEx + (exb & 1) * 512, sv, M.y,
-                             (long long)(U.row0 + cc) * M.N + U.nb * 128 + n, M.N, U.prow - cc, a.act);
-            exb++;
-          } else {
-            float* part = M.partial + ((long long)U.pass * M.P + U.gidx) * slab + (long long)cc * M.N + U.nb * 128 + n;
-#pragma unroll
-            for (int e = 0; e < 4; e++)
-              if (cc + e < U.prow) part[(long long)e * M.N] = v[e];
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&fold_done[gc & 1]);
-      }
-      if (!run) break;
-      if (M.P > 1) {
-        // publish the slab; the last of the block's P units folds the slabs and rotates back
-        fold_bar();
-        if (warp == kTcFoldWarp0 && lane == 0) {
-          __threadfence();
-          const int old = atomicAdd(&M.counters[U.pass * M.NB + U.nb], 1);
-          const bool last = old == M.arrivals - 1;
-          if (last) __threadfence();
-          s_last = last;
-        }
-        fold_bar();
-        if (s_last) {
-          const float* base = M.partial + (long long)U.pass * M.P * slab + U.nb * 128 + n;
-          for (int cc = 0; cc < U.prow; cc += 4) {
+        const bool ok = fold_all(wait_lane0(&chunk_done[gc & 1], (gc >> 1) & 1, &s_abort, ta.err, lane, 64));
+        if (ok) {
+          tc_fence_after();
+          const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * NMf);
+          const bool final = c + 1 == M.G;
+          for (int cc = 0; cc < U.NMp; cc += 4) {
             float v[4];
+            tmem_ld4(cur + (uint32_t)cc, v);
+            int l = 0;
+            for (; l < kTcMaxLevels && ((c >> l) & 1); l++) {
+              float w4[4];
+              tmem_ld4(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), w4);
 #pragma unroll
-            for (int e = 0; e < 4; e++)
-              v[e] = cc + e < U.prow ? tree_load<true>(base + (long long)(cc + e) * M.N, slab, M.P) : 0.f;
-            tc_rot_out_store(v, n, lane, sEx + (exb & 1) * 512, sv, M.y,
-                             (long long)(U.row0 + cc) * M.N + U.nb * 128 + n, M.N, U.prow - cc, a.act);
-            exb++;
+              for (int e = 0; e < 4; e++) v[e] = w4[e] + v[e];
+            }
+            if (!final) {
+              tmem_st4(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), v);
+            } else if (M.P == 1) {
+              tc_rot_out_store(v, n, lane, sEx + (exb & 1) * 512, sv, M.y,
+                               (long long)(U.row0 + cc) * M.N + U.nb * 128 + n, M.N, U.prow - cc, a.act);
+              exb++;
+            } else {
+              float* part =
+                  M.partial + ((long long)U.pass * M.P + U.gidx) * slab + (long long)cc * M.N + U.nb * 128 + n;
+#pragma unroll
+              for (int e = 0; e < 4; e++)
+                if (cc + e < U.prow) part[(long long)e * M.N] = v[e];
+            }
           }
-          if (warp == kTcFoldWarp0 && lane == 0) M.counters[U.pass * M.NB + U.nb] = 0;
+          tc_fence_before();
         }
-        fold_bar();
+        bar_arrive(kBarFolded + (gc & 1), kFoldedThreads);
       }
     }
   } else if (warp == kTcMmaWarp) {
-    // ---------------- MMA issue, strictly in k order
-    if (lane == 0) {
-      // descriptors advance by (byte offset >> 4) within the 256 KB shared window
-      const uint64_t da0 = umma_desc(sA), db0 = umma_desc(sX);
-      int gs = 0, gc = -1;
-      bool run = true;
-      for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
-        const TcUnit U = tc_unit(ta, u);
-        const Member& M = a.m[U.mi];
-        const uint32_t idesc = umma_idesc(U.NMp);
-        const int log2C = __ffs(M.C) - 1;
-        const int c0 = U.gidx * M.G;
-        int ci = -1, cnext = 0;
-        uint32_t acc = 0, dcol = 0;
-        for (int s0 = 0; run && s0 < U.nsteps; s0 += kTcSK, gs++) {
-          const int cnt = min(kTcSK, U.nsteps - s0);
-          const int ab = gs % kTcAB, xs = gs % kTcXS;
-          if (!mbar_wait(&aready[ab], (gs / kTcAB) & 1, &s_abort, ta.err) ||
-              !mbar_wait(&xfull[xs], (gs / kTcXS) & 1, &s_abort, ta.err)) {
-            run = false;
-            break;
+    // ---------------- MMA issue, strictly in k order; lane 0 issues, the warp takes the barriers
+    const int total = tc_stages_of_cta(ta);
+    const uint64_t da0 = umma_desc(sA), db0 = umma_desc(sX);
+    int gs = 0, gc = -1;
+    for (int u = blockIdx.x; u < ta.units; u += gridDim.x) {
+      const TcUnit U = tc_unit(ta, u);
+      const Member& M = a.m[U.mi];
+      const uint32_t idesc = umma_idesc(U.NMp);
+      const int log2C = __ffs(M.C) - 1;
+      const int c0 = U.gidx * M.G;
+      int ci = -1, cnext = 0;
+      uint32_t acc = 0, dcol = 0;
+      for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
+        const int cnt = min(kTcSK, U.nsteps - s0);
+        const int ab = gs % kTcAB, xs = gs % kTcXS;
+        bar_sync(kBarReady + ab, kReadyThreads);
+        int okx = 1;
+        if (lane == 0) okx = mbar_wait(&xfull[xs], (gs / kTcXS) & 1, &s_abort, ta.err);
+        okx = __shfl_sync(0xffffffffu, okx, 0);
+        tc_fence_after();
+        uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
+        uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
+        const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
+        for (int q = 0; q < cnt; q++) {
+          const int i = s0 + q;
+          if (i == cnext) {
+            ci++;
+            gc++;
+            acc = 0;
+            dcol = (uint32_t)((gc & 1) * NMf);
+            cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
+            // the region of chunk gc last held chunk gc-2: it must have been folded
+            if (gc >= 2) bar_sync(kBarFolded + (gc & 1), kFoldedThreads);
+            tc_fence_after();
           }
-          tc_fence_after();
-          uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
-          uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
-          const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
-          for (int q = 0; q < cnt; q++) {
-            const int i = s0 + q;
-            if (i == cnext) {
-              ci++;
-              gc++;
-              acc = 0;
-              dcol = (uint32_t)((gc & 1) * NMf);
-              cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
-              // the region of chunk gc last held chunk gc-2: it must have been folded
-              if (gc >= 2 && !mbar_wait(&fold_done[gc & 1], ((gc - 2) >> 1) & 1, &s_abort, ta.err)) {
-                run = false;
-                break;
-              }
-              tc_fence_after();
-            }
-            umma_f16(tmem + dcol, da, db, idesc, acc);
-            acc = 1;
-            if (i + 1 == cnext) umma_commit(&chunk_done[gc & 1]);
-            da += 4096 >> 4;
-            db += db_step;
-          }
-          if (!run) break;
-          umma_commit(&afree[ab]);
+          if (lane == 0 && okx && !s_abort) umma_f16(tmem + dcol, da, db, idesc, acc);
+          acc = 1;
+          if (lane == 0 && i + 1 == cnext) umma_commit(&chunk_done[gc & 1]);
+          da += 4096 >> 4;
+          db += db_step;
+        }
+        if (lane == 0) {
+          umma_commit(&amma[ab]);
           umma_commit(&xfree[xs]);
+        }
+        __syncwarp();
+        // release the A buffer of the previous stage once its MMAs are done
+        const int r = gs - 1;
+        if (r >= 0 && r + kTcAB < total) {
+          if (lane == 0) mbar_wait(&amma[r % kTcAB], (r / kTcAB) & 1, &s_abort, ta.err);
+          __syncwarp();
+          bar_arrive(kBarFree + r % kTcAB, kReadyThreads);
         }
       }
     }
-  } else if (warp == kTcWWarp) {
-    // ---------------- weight words: kTcSK tile rows of the block per stage
+    // the last stage's buffer, then the folds of the last two chunks
+    {
+      const int r = gs - 1;
+      if (r >= 0 && r + kTcAB < total) bar_arrive(kBarFree + r % kTcAB, kReadyThreads);
+    }
+    for (int c = gc - 1; c <= gc; c++)
+      if (c >= 0) bar_sync(kBarFolded + (c & 1), kFoldedThreads);
+  } else {
+    // ---------------- x rows of the pass: one contiguous run per stage
     if (lane == 0) {
       int gs = 0;
-      bool run = true;
-      for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
+      for (int u = blockIdx.x; u < ta.units; u += gridDim.x) {
         const TcUnit U = tc_unit(ta, u);
         const Member& M = a.m[U.mi];
-        const uint32_t* wsrc = M.trellis + (long long)U.nb * (64 * BITS);
+        const unsigned char* xsrc =
+            reinterpret_cast<const unsigned char*>(M.xf) + (long long)U.pass * ta.RP * a.K * 2;
         for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
           const int cnt = min(kTcSK, U.nsteps - s0);
-          const int ws = gs % kWS;
-          if (gs >= kWS && !mbar_wait(&wfree[ws], ((gs - kWS) / kWS) & 1, &s_abort, ta.err, 32)) {
-            run = false;
-            break;
-          }
-          mbar_expect_tx(&wfull[ws], (uint32_t)(cnt * WG::kRow));
-          for (int q = 0; q < cnt; q++)
-            bulk_g2s(sW + ws * WG::kStage + q * WG::kRow, wsrc + (long long)(U.tbeg + s0 + q) * M.stride, WG::kRow,
-                     &wfull[ws]);
+          const int xs = gs % kTcXS;
+          if (gs >= kTcXS && !mbar_wait(&xfree[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, 32)) continue;
+          if (s_abort) continue;
+          const uint32_t bytes = (uint32_t)(cnt * U.NMp * 32);
+          mbar_expect_tx(&xfull[xs], bytes);
+          bulk_g2s(sX + xs * kTcXStage, xsrc + (long long)(U.tbeg + s0) * U.NMp * 32, bytes, &xfull[xs]);
         }
       }
       if (s_abort) {
@@ -526,34 +520,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         }
       }
     }
-  } else {
-    // ---------------- x rows of the pass: one contiguous run per stage
-    if (lane == 0) {
-      int gs = 0;
-      bool run = true;
-      for (int u = blockIdx.x; run && u < ta.units; u += gridDim.x) {
-        const TcUnit U = tc_unit(ta, u);
-        const Member& M = a.m[U.mi];
-        const unsigned char* xsrc =
-            reinterpret_cast<const unsigned char*>(M.xf) + (long long)U.pass * ta.RP * a.K * 2;
-        for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
-          const int cnt = min(kTcSK, U.nsteps - s0);
-          const int xs = gs % kTcXS;
-          if (gs >= kTcXS && !mbar_wait(&xfree[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, 32)) {
-            run = false;
-            break;
-          }
-          const uint32_t bytes = (uint32_t)(cnt * U.NMp * 32);
-          mbar_expect_tx(&xfull[xs], bytes);
-          bulk_g2s(sX + xs * kTcXStage, xsrc + (long long)(U.tbeg + s0) * U.NMp * 32, bytes, &xfull[xs]);
-        }
-      }
-      if (s_abort) {
-        const long long t0 = clock64();
-        while (clock64() - t0 < 2000000) {
-        }
-      }
-    }
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -562,5 +529,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
   }
 }
+
+// Split-K combine of the tensor-core kernel's slabs when a block has P > 1
+// chunk groups: one warp per (pass, row, 128-column block) folds the P slabs
+// as a tree, rotates back (FWHT, 1/sqrt(128)), scales by svh and stores y:
+// the same arithmetic, in the same order, as block_epilogue.
+struct CombineArgs {
+  LinearArgs la;
+  int RP;
+  long long items[3];  // warps of each member (rows * NB); prefix over members
+};
+
+// tc_combine_kernel (defined once, in exl3_host.cu).
 
 }  // namespace tfx

@@ -151,8 +151,10 @@ typedef struct {
 int tfx_exl3_debug_set_driver(const tfx_exl3_driver* d);
 
 /* Device error word of a reserved weight: 1 once a tensor-core launch on it
- * gave up a bounded wait (a broken pipeline, never expected), 0 otherwise.
- * Synchronous copy; for tests and diagnostics. reset_counters clears it. */
+ * gave up a bounded wait (a broken pipeline, never expected), 2 if it was
+ * launched with less shared memory than it lays out (it then does nothing),
+ * 0 otherwise. Synchronous copy; for tests and diagnostics. reset_counters
+ * clears it. */
 int tfx_exl3_debug_error(const tfx_exl3_weight* w, int* device_error);
 
 /* Measurement hook: the next linear/group call on this thread records
