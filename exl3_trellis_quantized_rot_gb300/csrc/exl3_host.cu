@@ -38,43 +38,13 @@ __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArg
   if (item >= (long long)a.rows_pad * nblk) return;
   const int r = (int)(item / nblk);
   const int b = (int)(item % nblk);
-  float xv[4] = {0.f, 0.f, 0.f, 0.f};
-  if (r < a.rows) {
-    const long long base = (long long)r * a.K + 128LL * b + 4 * lane;
-    if (a.act == 0) {
-      uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(a.x) + base);
-      __half2 h0 = *reinterpret_cast<__half2*>(&u.x), h1 = *reinterpret_cast<__half2*>(&u.y);
-      xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
-    } else {
-      uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + base);
-      __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&u.x), h1 = *reinterpret_cast<__nv_bfloat162*>(&u.y);
-      xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
-    }
-  }
-  // element k = 128b + 4*lane + e sits in tile 8b + lane/4 at kk = 4*(lane%4) + e;
-  // the pair (kk, kk+1) for kk = 4*(lane%4) + 2m belongs to fragment lane 4g + 2*(lane%2) + m,
-  // register (lane%4) >= 2 (the k+8 half)
-  const int TK = a.K / 16;
-  const int q = r >> 3, gq = r & 7;
-  const int tk = 8 * b + (lane >> 2);
-  const int reg = (lane & 3) >= 2 ? 1 : 0;
+  float xv[4];
+  rot_load(a, r, b, lane, xv);
   for (int m = 0; m < a.count; m++) {
-    uint2 su = *reinterpret_cast<const uint2*>(a.suh[m] + 128LL * b + 4 * lane);
-    __half2 s0 = *reinterpret_cast<__half2*>(&su.x), s1 = *reinterpret_cast<__half2*>(&su.y);
-    float v[4] = {xv[0] * __low2float(s0), xv[1] * __high2float(s0), xv[2] * __low2float(s1),
-                  xv[3] * __high2float(s1)};
-    fwht128(v, lane);
     __half2 h[2];
-#pragma unroll
-    for (int mm = 0; mm < 2; mm++)
-      h[mm] = __halves2half2(__float2half_rn(v[2 * mm] * kInvSqrt128), __float2half_rn(v[2 * mm + 1] * kInvSqrt128));
+    rot_member(a, m, b, lane, xv, h);
     if (a.layout == 0) {
-      uint32_t* out = reinterpret_cast<uint32_t*>(a.xf[m]);
-#pragma unroll
-      for (int mm = 0; mm < 2; mm++) {
-        const int fl = 4 * gq + 2 * (lane & 1) + mm;
-        out[xf_index(q, tk, fl, TK) * 2 + reg] = *reinterpret_cast<uint32_t*>(&h[mm]);
-      }
+      rot_store_frag(a, m, r, b, lane, h);
     } else {
       // the lane's 4 values are k%8 = 4*(lane%2) .. +3 of one core-matrix row: one 8-byte store
       uint2 o;
@@ -99,33 +69,7 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__
   if (mi >= a.count) return;
   const Member& M = a.m[mi];
   if (M.P <= 1) return;
-  const int r = (int)(w / M.NB), nb = (int)(w % M.NB);  // r: row of the call
-  const int pass = r / ca.RP, rr = r - pass * ca.RP;
-  const int n0 = nb * 128 + 4 * lane;
-  const long long slab = (long long)a.rp * M.N;
-  const float* base = M.partial + (long long)pass * M.P * slab + (long long)rr * M.N + n0;
-  float v[4];
-#pragma unroll
-  for (int e = 0; e < 4; e++) v[e] = tree_load<true>(base + e, slab, M.P);
-  fwht128(v, lane);
-  float sv[4];
-#pragma unroll
-  for (int e = 0; e < 4; e++) sv[e] = __half2float(M.svh[n0 + e]);
-#pragma unroll
-  for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
-  const long long yo = (long long)r * M.N + n0;
-  uint2 out;
-  if (a.act == 0) {
-    __half2 o0 = __floats2half2_rn(v[0], v[1]), o1 = __floats2half2_rn(v[2], v[3]);
-    out.x = *reinterpret_cast<uint32_t*>(&o0);
-    out.y = *reinterpret_cast<uint32_t*>(&o1);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(M.y) + yo) = out;
-  } else {
-    __nv_bfloat162 o0 = __floats2bfloat162_rn(v[0], v[1]), o1 = __floats2bfloat162_rn(v[2], v[3]);
-    out.x = *reinterpret_cast<uint32_t*>(&o0);
-    out.y = *reinterpret_cast<uint32_t*>(&o1);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(M.y) + yo) = out;
-  }
+  combine_item(a, M, (int)(w / M.NB), (int)(w % M.NB), ca.RP, lane);
 }
 
 }  // namespace tfx
@@ -277,21 +221,25 @@ int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, v
 }
 
 // The linear kernel family for `rows` rows.
+enum Kind { kRowsCta = 0, kRowsWarp = 1, kTensor = 2 };
 struct Family {
   const void* fn;
-  int wpc, nr;
-  bool rows;  // the decode-rows kernel; otherwise the tensor-core kernel
+  int wpc;   // warps per CTA
+  int ncol;  // tile-columns per warp (warp-granular kernel)
+  Kind kind;
+  bool rows() const { return kind != kTensor; }
 };
+
+int row_tile(int rows) { return rows <= 8 ? 0 : rows <= 16 ? 1 : rows <= 32 ? 2 : 3; }
 
 Family pick(int bits, int rows) {
   const tfx::KernelSet& ks = kernels(bits);
-  if (g_variant != 2 && rows <= 16)
-    return rows <= 8 ? Family{ks.linear_rows[0], tfx::kRowsTC * tfx::kRowsGW, 1, true}
-                     : Family{ks.linear_rows[1], tfx::kRowsTC * tfx::kRowsGW, 2, true};
-  if (g_variant != 2 && rows <= tfx::kRowsMaxRows)
-    return rows <= 32 ? Family{ks.linear_rows[2], tfx::kRowsTC * tfx::kRowsGW, 4, true}
-                      : Family{ks.linear_rows[3], tfx::kRowsTC * tfx::kRowsGW, 8, true};
-  return Family{ks.linear_tc, tfx::kTcThreads / 32, 0, false};
+  if (g_variant != 2 && rows <= tfx::kRowsMaxRows) {
+    const int i = row_tile(rows);
+    if (g_variant == 1) return Family{ks.linear_rows[i], tfx::kRowsTC * tfx::kRowsGW, 1, kRowsCta};
+    return Family{ks.linear_warp[i], 1, i < 2 ? 2 : 1, kRowsWarp};
+  }
+  return Family{ks.linear_tc, tfx::kTcThreads / 32, 0, kTensor};
 }
 
 // Tensor-core kernel: rows per pass, and chunks per work unit (G). Up to 128
@@ -402,7 +350,16 @@ int chunks_of(int K) {
   return c;
 }
 
-size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows) { return (size_t)((rows + 15) / 16 * 16) * w->K * 2; }
+// Rows of rotated x a call lays out: the decode-rows kernels read whole row
+// tiles of 8*NR rows (16, 16, 32, 64), the tensor-core kernel 16-row groups;
+// the rows past `rows` are written as zeros.
+int x_rows_padded(int rows) {
+  const int r16 = (rows + 15) / 16 * 16;
+  if (rows > kRowsMaxRows) return r16;
+  return rows <= 16 ? 16 : rows <= 32 ? 32 : 64;
+}
+
+size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows) { return (size_t)x_rows_padded(rows) * w->K * 2; }
 
 size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
   const int C = chunks_of(w->K), TN = w->N / 16;
@@ -436,18 +393,20 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ra.count = count;
   ra.rows = rows;
   ra.rows_pad = (rows + 15) / 16 * 16;
+  const Family f = pick(bits, rows);
+  if (f.rows()) ra.rows_pad = tfx::x_rows_padded(rows);  // whole row tiles, zero-padded
   ra.K = K;
   ra.act = ws[0]->act;
   for (int i = 0; i < count; i++) {
     ra.suh[i] = reinterpret_cast<const __half*>(ws[i]->suh);
     ra.xf[i] = sc.xf[i];
   }
-  const Family f = pick(bits, rows);
-  ra.layout = f.rows ? 0 : 1;
+  ra.layout = f.rows() ? 0 : 1;
   ra.rp_tc = tc_rows_per_pass(rows);
   const long long items = (long long)ra.rows_pad * (K / 128);
-  int rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
-                  pdl);
+  int rc = 0;
+  rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
+              pdl);
   if (rc) return rc;
 
   // one grid over every member's CTAs
@@ -456,13 +415,13 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   la.K = K;
   la.TK = K / 16;
   la.rows = rows;
-  const int per_pass = f.rows ? kRowsPerPass : tc_rows_per_pass(rows);
+  const int per_pass = f.rows() ? kRowsPerPass : tc_rows_per_pass(rows);
   la.passes = (rows + per_pass - 1) / per_pass;
   la.rp = rows < per_pass ? rows : per_pass;
   la.act = ws[0]->act;
   long long ctas = 0;
   int tcG = 0;
-  if (!f.rows) {
+  if (!f.rows()) {
     long long blocks = 0;
     for (int i = 0; i < count; i++) blocks += ws[i]->N / 128;
     tcG = tc_group(blocks, rows, chunks_of(K), K / 16);
@@ -481,7 +440,14 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     m.NB = w->N / 128;
     m.C = chunks_of(K);
     m.cta_begin = (int)ctas;
-    if (f.rows) {
+    if (f.kind == kRowsWarp) {
+      // one warp per (ncol tile-columns, chunk): C slabs folded by the combine kernel
+      m.G = 1;
+      m.TC = f.ncol;
+      m.P = m.C;
+      m.arrivals = 0;
+      ctas += (long long)(w->N / 16 / f.ncol) * m.C;
+    } else if (f.kind == kRowsCta) {
       const int TN = w->N / 16;
       m.G = rows_group(TN, m.C, rows);
       m.TC = rows_gw(m.C);  // the decode-rows kernel reads its warp-group count here
@@ -499,7 +465,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     m.log2G = __builtin_ctz(m.G);
   }
   if (ctas > 0x7fffffffLL) return fail(TFX_EUNSUPPORTED, "grid of %lld CTAs", ctas);
-  const size_t smem = f.rows ? 0 : kTcDynSmem;
+  const size_t smem = f.rows() ? 0 : kTcDynSmem;
   rc = set_smem(f.fn, smem);
   if (rc) return rc;
   TcArgs ta;
@@ -508,17 +474,17 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ta.RP = per_pass;
   ta.NMf = per_pass < ra.rows_pad ? per_pass : ra.rows_pad;
   ta.err = sc.err;
-  if (!f.rows) {
+  if (!f.rows()) {
     const long long S = sm_count();
     ctas = ctas < S ? ctas : S;  // persistent: one CTA per SM at most
   }
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && cudaEventRecord(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
-  rc = f.rows ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl)
-              : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
+  rc = f.rows() ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl)
+                : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
   if (rc) return rc;
-  if (!f.rows) {
+  if (f.kind == kRowsWarp || f.kind == kTensor) {
     // members split over P > 1 units: fold their slabs, one warp per (row, block)
     CombineArgs ca = {};
     ca.la = la;

@@ -161,6 +161,87 @@ __device__ __forceinline__ void fwht128(float (&v)[4], int lane) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Pieces of the input rotation and of the split-K combine shared by the
+// standalone kernels and the fused decode-rows kernel (same arithmetic, same
+// order, hence the same bits).
+
+// x[r][128b + 4*lane .. +3] as FP32 (zeros for padding rows r >= rows).
+__device__ __forceinline__ void rot_load(const RotArgs& a, int r, int b, int lane, float (&xv)[4]) {
+  xv[0] = xv[1] = xv[2] = xv[3] = 0.f;
+  if (r >= a.rows) return;
+  const long long base = (long long)r * a.K + 128LL * b + 4 * lane;
+  if (a.act == 0) {
+    uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(a.x) + base);
+    __half2 h0 = *reinterpret_cast<__half2*>(&u.x), h1 = *reinterpret_cast<__half2*>(&u.y);
+    xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
+  } else {
+    uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + base);
+    __nv_bfloat162 h0 = *reinterpret_cast<__nv_bfloat162*>(&u.x), h1 = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+    xv[0] = __low2float(h0); xv[1] = __high2float(h0); xv[2] = __low2float(h1); xv[3] = __high2float(h1);
+  }
+}
+
+// fp16(Hn(suh_m o x)) of one 128-block, the lane's 4 values as two half2.
+__device__ __forceinline__ void rot_member(const RotArgs& a, int m, int b, int lane, const float (&xv)[4],
+                                           __half2 (&h)[2]) {
+  uint2 su = *reinterpret_cast<const uint2*>(a.suh[m] + 128LL * b + 4 * lane);
+  __half2 s0 = *reinterpret_cast<__half2*>(&su.x), s1 = *reinterpret_cast<__half2*>(&su.y);
+  float v[4] = {xv[0] * __low2float(s0), xv[1] * __high2float(s0), xv[2] * __low2float(s1), xv[3] * __high2float(s1)};
+  fwht128(v, lane);
+#pragma unroll
+  for (int mm = 0; mm < 2; mm++)
+    h[mm] = __halves2half2(__float2half_rn(v[2 * mm] * kInvSqrt128), __float2half_rn(v[2 * mm + 1] * kInvSqrt128));
+}
+
+// Store in B-fragment order: element k = 128b + 4*lane + e sits in tile 8b + lane/4
+// at kk = 4*(lane%4) + e; the pair (kk, kk+1) for kk = 4*(lane%4) + 2m belongs to
+// fragment lane 4g + 2*(lane%2) + m, register (lane%4) >= 2 (the k+8 half).
+__device__ __forceinline__ void rot_store_frag(const RotArgs& a, int m, int r, int b, int lane, const __half2 (&h)[2]) {
+  const int TK = a.K / 16;
+  const int q = r >> 3, gq = r & 7;
+  const int tk = 8 * b + (lane >> 2);
+  const int reg = (lane & 3) >= 2 ? 1 : 0;
+  uint32_t* out = reinterpret_cast<uint32_t*>(a.xf[m]);
+#pragma unroll
+  for (int mm = 0; mm < 2; mm++) {
+    const int fl = 4 * gq + 2 * (lane & 1) + mm;
+    out[xf_index(q, tk, fl, TK) * 2 + reg] = *reinterpret_cast<const uint32_t*>(&h[mm]);
+  }
+}
+
+// Row r of the call, 128-column block nb of member M: fold the P slabs
+// [pass][P][rp][N] as a balanced tree, rotate back (FWHT, 1/sqrt(128)), scale
+// by svh, store y. One warp.
+__device__ __forceinline__ void combine_item(const LinearArgs& a, const Member& M, int r, int nb, int RP, int lane) {
+  const int pass = r / RP, rr = r - pass * RP;
+  const int n0 = nb * 128 + 4 * lane;
+  const long long slab = (long long)a.rp * M.N;
+  const float* base = M.partial + (long long)pass * M.P * slab + (long long)rr * M.N + n0;
+  float v[4];
+#pragma unroll
+  for (int e = 0; e < 4; e++) v[e] = tree_load<true>(base + e, slab, M.P);
+  fwht128(v, lane);
+  float sv[4];
+#pragma unroll
+  for (int e = 0; e < 4; e++) sv[e] = __half2float(M.svh[n0 + e]);
+#pragma unroll
+  for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
+  const long long yo = (long long)r * M.N + n0;
+  uint2 out;
+  if (a.act == 0) {
+    __half2 o0 = __floats2half2_rn(v[0], v[1]), o1 = __floats2half2_rn(v[2], v[3]);
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(M.y) + yo) = out;
+  } else {
+    __nv_bfloat162 o0 = __floats2bfloat162_rn(v[0], v[1]), o1 = __floats2bfloat162_rn(v[2], v[3]);
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(M.y) + yo) = out;
+  }
+}
+
 // Words of one tile a lane needs: its 8 weights' windows span bits
 // [8*lane*BITS, 8*lane*BITS + 7*BITS + 16), at most 2 words for BITS <= 4
 // and 3 words above, counted from the word holding the first bit.
@@ -494,6 +575,105 @@ __global__ void __launch_bounds__(kRowsTC * kRowsGW * 32, MINB)
   if (threadIdx.x == 0) M.counters[nb] = 0;
 }
 
+// Warp-granular decode-rows kernel (1..64 rows, one pass): one warp = NCOL
+// adjacent tile-columns x one K chunk, one warp per CTA, so the hardware
+// spreads the work over the SMs in units of one chain (TK/C tiles) and no SM
+// carries a whole extra CTA of work. The trellis words of the first PF tiles
+// are requested before the wait on the rotation kernel (they do not depend on
+// it). The chain runs from zero like every chunk; its FP32 result is slab
+// `chunk` of P = C slabs, and tc_combine_kernel folds each block's C slabs as
+// the chunk tree prescribes (a balanced binary tree in chunk order), rotates
+// back and stores y.
+template <int BITS, int NR, int NCOL, int PF>
+__global__ void __launch_bounds__(32) linear_warp_kernel(const __grid_constant__ LinearArgs a) {
+  using WF = WordFetch<BITS>;
+  const int lane = threadIdx.x;
+  const Member& M = pick_member(a);
+  const int local = blockIdx.x - M.cta_begin;
+  const int chunk = local % M.C;
+  const int tn0 = (local / M.C) * NCOL;
+  const int t0 = chunk_begin(chunk, a.TK, M.C), n = chunk_begin(chunk + 1, a.TK, M.C) - t0;
+  LaneWindow<BITS> lw;
+  lw.init(lane);
+  const long long wstride = M.stride;
+  const uint32_t* tp = M.trellis + (long long)t0 * wstride + (long long)tn0 * (8 * BITS);
+  uint32_t own[PF][NCOL][WF::kOwn];
+#pragma unroll
+  for (int p = 0; p < PF; p++)
+    if (p < n)
+#pragma unroll
+      for (int c = 0; c < NCOL; c++) WF::load(tp + p * wstride + c * (8 * BITS), lw, lane, own[p][c]);
+  griddep_wait();
+  griddep_launch();
+  const long long xsq = 32LL * a.TK;
+  const uint2* xp = M.xf + xf_index(0, t0, lane, a.TK);
+  uint2 xr[PF][NR];
+#pragma unroll
+  for (int p = 0; p < PF; p++)
+    if (p < n)
+#pragma unroll
+      for (int q = 0; q < NR; q++) xr[p][q] = __ldg(xp + q * xsq + 32 * p);
+  float acc[NCOL][NR][4];
+#pragma unroll
+  for (int c = 0; c < NCOL; c++)
+#pragma unroll
+    for (int q = 0; q < NR; q++) acc[c][q][0] = acc[c][q][1] = acc[c][q][2] = acc[c][q][3] = 0.f;
+  auto step = [&](const uint32_t (&ow)[NCOL][WF::kOwn], const uint2 (&xc)[NR]) {
+#pragma unroll
+    for (int c = 0; c < NCOL; c++) {
+      uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
+      WF::gather(ow[c], lw, lane, raw);
+      lw.align(raw, win);
+      decode8<BITS>(win, af);
+#pragma unroll
+      for (int q = 0; q < NR; q++) mma16816(acc[c][q], af, xc[q].x, xc[q].y);
+    }
+  };
+  int tk = 0;
+  for (; tk + PF <= n; tk += PF) {
+#pragma unroll
+    for (int p = 0; p < PF; p++) {
+      uint32_t oc[NCOL][WF::kOwn];
+      uint2 xc[NR];
+#pragma unroll
+      for (int c = 0; c < NCOL; c++)
+#pragma unroll
+        for (int i = 0; i < WF::kOwn; i++) oc[c][i] = own[p][c][i];
+#pragma unroll
+      for (int q = 0; q < NR; q++) xc[q] = xr[p][q];
+      const int nx = tk + p + PF;
+      if (nx < n) {
+#pragma unroll
+        for (int c = 0; c < NCOL; c++) WF::load(tp + nx * wstride + c * (8 * BITS), lw, lane, own[p][c]);
+#pragma unroll
+        for (int q = 0; q < NR; q++) xr[p][q] = __ldg(xp + q * xsq + 32 * nx);
+      }
+      step(oc, xc);
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < PF; p++)
+    if (tk + p < n) step(own[p], xr[p]);
+  // slab `chunk`: lane (g, t) holds (row 8q + 2t | +1, column g | g + 8) of tile-column tn0 + c
+  const int g = lane >> 2, t = lane & 3;
+  float* part = M.partial + (long long)chunk * a.rp * M.N + (long long)tn0 * 16;
+#pragma unroll
+  for (int c = 0; c < NCOL; c++)
+#pragma unroll
+    for (int q = 0; q < NR; q++) {
+      const int r0 = 8 * q + 2 * t;
+      float* pc = part + c * 16 + g;
+      if (r0 < a.rows) {
+        pc[(long long)r0 * M.N] = acc[c][q][0];
+        pc[(long long)r0 * M.N + 8] = acc[c][q][2];
+      }
+      if (r0 + 1 < a.rows) {
+        pc[(long long)(r0 + 1) * M.N] = acc[c][q][1];
+        pc[(long long)(r0 + 1) * M.N + 8] = acc[c][q][3];
+      }
+    }
+}
+
 // Debug: decode every tile to W[k][n] (FP16). One warp per tile.
 template <int BITS>
 __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ DecodeArgs a) {
@@ -524,6 +704,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ Dec
 // Kernel pointers for one bit width (defined in exl3_bits.cu).
 struct KernelSet {
   const void* linear_rows[4];  // decode-rows family: NR = 1, 2, 4, 8 (8, 16, 32, 64 rows)
+  const void* linear_warp[4];  // warp-granular decode-rows kernel, same row tiles
   const void* linear_tc;       // tensor-core family: any row count, persistent
   const void* decode;
 };
