@@ -32,7 +32,12 @@ ROWS = 16
 QKV = (6144, 1024, 1024)
 O_N = 5120
 L2_BYTES = 129 * 1024 * 1024
-METRIC = "EXL3 linear weight-stream GB/s (µs/call alongside) vs HBM roofline, decode rows at 27B shapes"
+METRIC = "EXL3 linear \u00b5s/call & weight-stream GB/s vs HBM roofline, rows 1/16/64/128"
+
+
+# 152 SMs x 4 schedulers x 1 warp-instruction per clock x 2.07 GHz, 46.5
+# warp-instructions per 16x16 tile of the decode rule, 256 weights per tile
+ALU_DECODE_PEAK_GW = round(152 * 4 * 2.07e9 / 46.5 * 256 / 1e9, 1)
 
 
 def packed_bytes(Kk, N, bits):
@@ -297,8 +302,16 @@ def run_gpu(args):
         # packed codes + rotated x read + svh + y written (split-K scratch excluded)
         return sum(packed_bytes(K, n, BITS) + 2 * ROWS * K + 2 * n + 2 * ROWS * n for n in Ns)
 
-    achieved = (alg_bytes(QKV) + alg_bytes([O_N])) / ((grp_ms + one_ms) / 1e3) / 1e9
+    kern_s = (grp_ms + one_ms) / 1e3
+    hbm_achieved = (alg_bytes(QKV) + alg_bytes([O_N])) / kern_s / 1e9
     peak, peak_kind = load_peaks()
+    # the binding roofline at 4 bits is the decode arithmetic on the plain ALUs:
+    # weights decoded per second against the issue rate of 152 SMs x 4 schedulers
+    # at the maximum SM clock, at the rule's measured 46.5 warp-instructions per
+    # 256-weight tile
+    dec_weights = sum(K * n for n in QKV) + K * O_N
+    dec_achieved = dec_weights / kern_s / 1e9
+    dec_peak = ALU_DECODE_PEAK_GW
     traffic = None
     tp = os.path.join(ROOT, "profiles", "linear_kernel_traffic.json")
     if os.path.exists(tp):
@@ -416,14 +429,18 @@ def run_gpu(args):
                        "parallelism": f"replicas x{ws}"},
             "us_per_step": round(sec_per_step * 1e6, 3),
             "detail": detail,
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "kernel": "linear_rows_kernel<4,2,4,4> (decode rows), group + single launch",
-                         "peak_source": f"{peak_kind} hbm_gbs",
+            "roofline": {"bound": "alu", "achieved": round(dec_achieved, 1), "peak": dec_peak,
+                         "unit": "G decoded weights/s", "frac": round(dec_achieved / dec_peak, 4), "traffic": traffic,
+                         "kernel": "linear_warp_kernel<4,2,2,3> + tc_combine_kernel (decode rows), "
+                                   "group + single call",
+                         "peak_source": "derived: 152 SMs x 4 schedulers x 2.07 GHz / 46.5 warp-instructions "
+                                        "per 256-weight tile",
+                         "hbm": {"achieved": round(hbm_achieved, 1), "peak": peak, "unit": "GB/s",
+                                 "frac": round(hbm_achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs"},
                          "kernel_us": {"group": round(grp_ms * 1e3, 3), "single": round(one_ms * 1e3, 3)}},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * 2,
                     "d2h_bytes_per_step": sum(h.numel() * 2 for h in yh)},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 6 * args.steps,  # per call: rotation, decode-rows chains, combine
             "clocks": clocks,
         }
         if cpu is not None:

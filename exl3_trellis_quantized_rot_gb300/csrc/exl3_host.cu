@@ -237,7 +237,7 @@ Family pick(int bits, int rows) {
   if (g_variant != 2 && rows <= tfx::kRowsMaxRows) {
     const int i = row_tile(rows);
     if (g_variant == 1) return Family{ks.linear_rows[i], tfx::kRowsTC * tfx::kRowsGW, 1, kRowsCta};
-    return Family{ks.linear_warp[i], 1, i < 2 ? 2 : 1, kRowsWarp};
+    return Family{ks.linear_warp[i], tfx::kWarpCta, i < 2 ? 2 : 1, kRowsWarp};
   }
   return Family{ks.linear_tc, tfx::kTcThreads / 32, 0, kTensor};
 }
@@ -464,6 +464,8 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     }
     m.log2G = __builtin_ctz(m.G);
   }
+  la.items = ctas;
+  if (f.kind == kRowsWarp) ctas = (ctas + f.wpc - 1) / f.wpc;  // wpc independent warps per CTA
   if (ctas > 0x7fffffffLL) return fail(TFX_EUNSUPPORTED, "grid of %lld CTAs", ctas);
   const size_t smem = f.rows() ? 0 : kTcDynSmem;
   rc = set_smem(f.fn, smem);

@@ -72,6 +72,7 @@ struct LinearArgs {
   int passes;   // ceil(rows / 128)
   int rp;       // row stride of a partial slab = min(rows, 128)
   int act;      // 0 FP16, 1 BF16
+  long long items;  // work items of the warp-granular kernel (all members)
 };
 
 struct RotArgs {
@@ -370,12 +371,15 @@ __device__ __forceinline__ void block_epilogue(const Member& M, const LinearArgs
   }
 }
 
-__device__ __forceinline__ const Member& pick_member(const LinearArgs& a) {
+__device__ __forceinline__ const Member& pick_member_at(const LinearArgs& a, long long idx) {
   int mi = 0;
-  if (a.count > 1 && (int)blockIdx.x >= a.m[1].cta_begin) mi = 1;
-  if (a.count > 2 && (int)blockIdx.x >= a.m[2].cta_begin) mi = 2;
+  if (a.count > 1 && idx >= a.m[1].cta_begin) mi = 1;
+  if (a.count > 2 && idx >= a.m[2].cta_begin) mi = 2;
   return a.m[mi];
 }
+__device__ __forceinline__ const Member& pick_member(const LinearArgs& a) { return pick_member_at(a, blockIdx.x); }
+
+constexpr int kWarpCta = 1;  // warps (independent work items) per CTA of the warp-granular kernel
 
 // ---------------------------------------------------------------------------
 // Decode-rows kernel (1..64 rows in row tiles of 8*NR, one pass). One CTA = WPC warps = WPC
@@ -585,11 +589,13 @@ __global__ void __launch_bounds__(kRowsTC * kRowsGW * 32, MINB)
 // the chunk tree prescribes (a balanced binary tree in chunk order), rotates
 // back and stores y.
 template <int BITS, int NR, int NCOL, int PF>
-__global__ void __launch_bounds__(32) linear_warp_kernel(const __grid_constant__ LinearArgs a) {
+__global__ void __launch_bounds__(32 * kWarpCta) linear_warp_kernel(const __grid_constant__ LinearArgs a) {
   using WF = WordFetch<BITS>;
-  const int lane = threadIdx.x;
-  const Member& M = pick_member(a);
-  const int local = blockIdx.x - M.cta_begin;
+  const int lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * kWarpCta + (threadIdx.x >> 5);
+  if (item >= a.items) return;
+  const Member& M = pick_member_at(a, item);
+  const int local = (int)(item - M.cta_begin);
   const int chunk = local % M.C;
   const int tn0 = (local / M.C) * NCOL;
   const int t0 = chunk_begin(chunk, a.TK, M.C), n = chunk_begin(chunk + 1, a.TK, M.C) - t0;

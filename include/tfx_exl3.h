@@ -131,10 +131,13 @@ int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk);
 /* Allocations and counter memsets made for this weight since its creation. */
 int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
 
-/* Kernel family forced for the next calls: 0 = auto (1..16 rows decode-rows,
- * more rows the tensor-core kernel), 1 = decode-rows whenever rows <= 16,
- * 2 = the tensor-core kernel for every row count. The initial value comes from TFX_EXL3_VARIANT
- * (auto|rows|mid). Returns the previous value. */
+/* Kernel family for the next calls. 0 = auto: 1..64 rows the warp-granular
+ * decode-rows kernel (C FP32 slabs folded by a combine kernel), more rows the
+ * tensor-core kernel; 1 = for 1..64 rows the CTA decode-rows kernel whose
+ * split-K partials are summed in-kernel by the last CTA to arrive on each
+ * block's counter (the counter resets itself), more rows as auto; 2 = the
+ * tensor-core kernel for every row count. All give the same bytes. Initial
+ * value from TFX_EXL3_VARIANT (auto|rows|mid). Returns the previous value. */
 int tfx_exl3_set_variant(int variant);
 
 /* Programmatic dependent launch on (1) or off (0); initial value from

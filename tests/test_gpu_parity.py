@@ -95,15 +95,22 @@ def test_group_planted_controls_go_red(qkv):
     assert not same_bytes(bad[2], ref[2])
 
 
-def test_repeated_calls_need_no_memset():
-    hw, w = make(4, 5120, 1024, 4)  # 8 splits: every block goes through the counters
+@pytest.mark.parametrize("variant", [tfx.VARIANT_ROWS, tfx.VARIANT_AUTO])
+def test_repeated_calls_need_no_memset(variant):
+    # VARIANT_ROWS: every block goes through the in-kernel arrival counters (8 splits);
+    # VARIANT_AUTO: C slabs folded by the combine kernel
+    hw, w = make(4, 5120, 1024, 4)
     x64, x = x_of(4, 16, 5120)
-    first = tfx.linear(w, x)
-    allocs, memsets = tfx.stats(w)
-    y = torch.empty_like(first)
-    for _ in range(100):
-        tfx.linear(w, x, y=y)
-        assert same_bytes(y, first)
+    tfx.set_variant(variant)
+    try:
+        first = tfx.linear(w, x)
+        allocs, memsets = tfx.stats(w)
+        y = torch.empty_like(first)
+        for _ in range(100):
+            tfx.linear(w, x, y=y)
+            assert same_bytes(y, first)
+    finally:
+        tfx.set_variant(tfx.VARIANT_AUTO)
     assert tfx.stats(w) == (allocs, memsets) == (3, 1)
     assert tfx.device_error(w) == 0
     assert_close(to_f64(first), oracle_y(hw, x64), what="repeat")
@@ -126,10 +133,15 @@ def test_repeated_tensor_core_calls_need_no_memset():
 def test_reset_counters_then_same_bytes():
     hw, w = make(5, 5120, 1024, 4)
     x64, x = x_of(5, 3, 5120)
-    a = tfx.linear(w, x)
-    tfx.reset_counters(w)
-    b = tfx.linear(w, x)
+    tfx.set_variant(tfx.VARIANT_ROWS)
+    try:
+        a = tfx.linear(w, x)
+        tfx.reset_counters(w)
+        b = tfx.linear(w, x)
+    finally:
+        tfx.set_variant(tfx.VARIANT_AUTO)
     assert same_bytes(a, b)
+    assert same_bytes(a, tfx.linear(w, x))
 
 
 # ------------------------------------------------------------------ row independence, variants
@@ -152,7 +164,7 @@ def test_variants_and_row_counts_byte_identical(K, N, act):
     ref = tfx.linear(w, x)  # 128 rows: mid kernel, NR = 16
     try:
         for rows in (1, 7, 16, 17, 24, 32, 33, 48, 49, 64, 100, 128):
-            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_MID):
+            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID):
                 tfx.set_variant(var)
                 y = tfx.linear(w, x[:rows])
                 assert same_bytes(y, ref[:rows]), (rows, var)
@@ -254,7 +266,7 @@ def test_nan_and_inf_reach_their_rows_only():
     xb[2, 5] = float("nan")
     xb[3, 700] = float("inf")
     xb[5, 1] = float("-inf")
-    for var in (tfx.VARIANT_AUTO, tfx.VARIANT_MID):
+    for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID):
         tfx.set_variant(var)
         try:
             y = tfx.linear(w, xb)
