@@ -344,73 +344,74 @@ def run_gpu(args):
 
     # per-row-count µs/call (extra detail), same cycling of copies
     detail = {}
+    if not args.no_detail:
 
-    def time_calls(fn, n_calls):
-        for i in range(3):
-            fn(i)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(n_calls):
-            fn(i)
-        b.record(stream)
+        def time_calls(fn, n_calls):
+            for i in range(3):
+                fn(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(n_calls):
+                fn(i)
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) * 1e3 / n_calls
+
+        for rows in (1, 7, 16):
+            xr_ = x[:rows]
+            detail[f"qkv_group_rows{rows}_us"] = round(time_calls(
+                lambda i, xr_=xr_, rows=rows: tfx.group(sets[i % copies][:3], xr_, rows, [y[:rows] for y in ys], stream),
+                max(20, args.steps)), 3)
+            detail[f"single_5120_rows{rows}_us"] = round(time_calls(
+                lambda i, xr_=xr_, rows=rows: tfx.linear(sets[i % copies][3], xr_, rows, yo[:rows], stream),
+                max(20, args.steps)), 3)
+
+        # mid rows on the 5120x5120 weight (same copies, reserved for 128 rows)
+        x128 = torch.from_numpy(synth.activations(2000 + rank, 128, K, "f16")).to(dev)
+        y128 = torch.empty((128, O_N), dtype=torch.float16, device=dev)
+        for c in range(copies):
+            tfx.reserve(sets[c][3], 128, stream)
+        for rows in (64, 128):
+            us = time_calls(lambda i, rows=rows: tfx.linear(sets[i % copies][3], x128[:rows], rows, y128[:rows], stream),
+                            max(20, args.steps))
+            detail[f"single_5120_rows{rows}_us"] = round(us, 3)
+            detail[f"single_5120_rows{rows}_tflops"] = round(2 * rows * K * O_N / us / 1e6, 1)
+
+        # gate+up group (K = 5120, N = 17408 each, BF16 activations) at mid rows and a 4096-row chunk
+        GU = 17408
+        gu_bytes = 2 * packed_bytes(K, GU, BITS)
+        gu_copies = max(2, -(-4 * L2_BYTES // gu_bytes))
+        gbase = []
+        for m in range(2):
+            codes = synth.codes(3000 + rank, K, GU, BITS, m)
+            gbase.append((torch.from_numpy(codes.view(np.int32)).to(dev),
+                          torch.from_numpy(synth.suh(3000 + rank, K, m).view(np.int16)).to(dev),
+                          torch.from_numpy(synth.svh(3000 + rank, GU, m).view(np.int16)).to(dev)))
+        gsets = []
+        for c in range(gu_copies):
+            pair = []
+            for (t, su, sv) in gbase:
+                wc = tfx.Weight(t.clone() if c else t, su, sv, K, GU, BITS, tfx.BF16)
+                tfx.reserve(wc, 128, stream)
+                pair.append(wc)
+            gsets.append(pair)
+        xb = torch.from_numpy(synth.activations(3000 + rank, 128, K, "bf16").view(np.int16)).to(dev).view(torch.bfloat16)
+        gys = [torch.empty((128, GU), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        for rows in (1, 16, 64, 128):
+            us = time_calls(lambda i, rows=rows: tfx.group(gsets[i % gu_copies], xb[:rows], rows,
+                                                           [y[:rows] for y in gys], stream), 20)
+            detail[f"gate_up_rows{rows}_us"] = round(us, 3)
+            detail[f"gate_up_rows{rows}_GBps"] = round(gu_bytes / us / 1e3, 1)
+            detail[f"gate_up_rows{rows}_tflops"] = round(2 * rows * K * 2 * GU / us / 1e6, 1)
+        del gsets
+        gate = tfx.Weight(gbase[0][0], gbase[0][1], gbase[0][2], K, GU, BITS, tfx.BF16)
+        tfx.reserve(gate, 4096, stream)
+        x4k = torch.from_numpy(synth.activations(4000 + rank, 4096, K, "bf16").view(np.int16)).to(dev).view(torch.bfloat16)
+        y4k = torch.empty((4096, GU), dtype=torch.bfloat16, device=dev)
+        us = time_calls(lambda i: tfx.linear(gate, x4k, 4096, y4k, stream), 5)
+        detail["gate_rows4096_us"] = round(us, 1)
+        detail["gate_rows4096_tflops"] = round(2 * 4096 * K * GU / us / 1e6, 1)
         torch.cuda.synchronize()
-        return a.elapsed_time(b) * 1e3 / n_calls
-
-    for rows in (1, 7, 16):
-        xr_ = x[:rows]
-        detail[f"qkv_group_rows{rows}_us"] = round(time_calls(
-            lambda i, xr_=xr_, rows=rows: tfx.group(sets[i % copies][:3], xr_, rows, [y[:rows] for y in ys], stream),
-            max(20, args.steps)), 3)
-        detail[f"single_5120_rows{rows}_us"] = round(time_calls(
-            lambda i, xr_=xr_, rows=rows: tfx.linear(sets[i % copies][3], xr_, rows, yo[:rows], stream),
-            max(20, args.steps)), 3)
-
-    # mid rows on the 5120x5120 weight (same copies, reserved for 128 rows)
-    x128 = torch.from_numpy(synth.activations(2000 + rank, 128, K, "f16")).to(dev)
-    y128 = torch.empty((128, O_N), dtype=torch.float16, device=dev)
-    for c in range(copies):
-        tfx.reserve(sets[c][3], 128, stream)
-    for rows in (64, 128):
-        us = time_calls(lambda i, rows=rows: tfx.linear(sets[i % copies][3], x128[:rows], rows, y128[:rows], stream),
-                        max(20, args.steps))
-        detail[f"single_5120_rows{rows}_us"] = round(us, 3)
-        detail[f"single_5120_rows{rows}_tflops"] = round(2 * rows * K * O_N / us / 1e6, 1)
-
-    # gate+up group (K = 5120, N = 17408 each, BF16 activations) at mid rows and a 4096-row chunk
-    GU = 17408
-    gu_bytes = 2 * packed_bytes(K, GU, BITS)
-    gu_copies = max(2, -(-4 * L2_BYTES // gu_bytes))
-    gbase = []
-    for m in range(2):
-        codes = synth.codes(3000 + rank, K, GU, BITS, m)
-        gbase.append((torch.from_numpy(codes.view(np.int32)).to(dev),
-                      torch.from_numpy(synth.suh(3000 + rank, K, m).view(np.int16)).to(dev),
-                      torch.from_numpy(synth.svh(3000 + rank, GU, m).view(np.int16)).to(dev)))
-    gsets = []
-    for c in range(gu_copies):
-        pair = []
-        for (t, su, sv) in gbase:
-            wc = tfx.Weight(t.clone() if c else t, su, sv, K, GU, BITS, tfx.BF16)
-            tfx.reserve(wc, 128, stream)
-            pair.append(wc)
-        gsets.append(pair)
-    xb = torch.from_numpy(synth.activations(3000 + rank, 128, K, "bf16").view(np.int16)).to(dev).view(torch.bfloat16)
-    gys = [torch.empty((128, GU), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    for rows in (1, 16, 64, 128):
-        us = time_calls(lambda i, rows=rows: tfx.group(gsets[i % gu_copies], xb[:rows], rows,
-                                                       [y[:rows] for y in gys], stream), 20)
-        detail[f"gate_up_rows{rows}_us"] = round(us, 3)
-        detail[f"gate_up_rows{rows}_GBps"] = round(gu_bytes / us / 1e3, 1)
-        detail[f"gate_up_rows{rows}_tflops"] = round(2 * rows * K * 2 * GU / us / 1e6, 1)
-    del gsets
-    gate = tfx.Weight(gbase[0][0], gbase[0][1], gbase[0][2], K, GU, BITS, tfx.BF16)
-    tfx.reserve(gate, 4096, stream)
-    x4k = torch.from_numpy(synth.activations(4000 + rank, 4096, K, "bf16").view(np.int16)).to(dev).view(torch.bfloat16)
-    y4k = torch.empty((4096, GU), dtype=torch.bfloat16, device=dev)
-    us = time_calls(lambda i: tfx.linear(gate, x4k, 4096, y4k, stream), 5)
-    detail["gate_rows4096_us"] = round(us, 1)
-    detail["gate_rows4096_tflops"] = round(2 * 4096 * K * GU / us / 1e6, 1)
-    torch.cuda.synchronize()
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -467,6 +468,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-detail", action="store_true", help="skip the per-row-count detail timings")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -213,15 +213,38 @@ __device__ __forceinline__ void rot_store_frag(const RotArgs& a, int m, int r, i
 
 // Row r of the call, 128-column block nb of member M: fold the P slabs
 // [pass][P][rp][N] as a balanced tree, rotate back (FWHT, 1/sqrt(128)), scale
-// by svh, store y. One warp.
+// by svh, store y. One warp; the lane's 4 columns of every slab come in one
+// 16-byte load, all P loads in flight at once.
+template <int P>
+__device__ __forceinline__ void combine_fold(const float* base, long long slab, float (&v)[4]) {
+  float4 s[P];
+#pragma unroll
+  for (int p = 0; p < P; p++) s[p] = __ldcg(reinterpret_cast<const float4*>(base + p * slab));
+  float t[4][P];
+#pragma unroll
+  for (int p = 0; p < P; p++) {
+    t[0][p] = s[p].x;
+    t[1][p] = s[p].y;
+    t[2][p] = s[p].z;
+    t[3][p] = s[p].w;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; e++) v[e] = tree_sum<P>(t[e]);
+}
+
 __device__ __forceinline__ void combine_item(const LinearArgs& a, const Member& M, int r, int nb, int RP, int lane) {
   const int pass = r / RP, rr = r - pass * RP;
   const int n0 = nb * 128 + 4 * lane;
   const long long slab = (long long)a.rp * M.N;
   const float* base = M.partial + (long long)pass * M.P * slab + (long long)rr * M.N + n0;
   float v[4];
-#pragma unroll
-  for (int e = 0; e < 4; e++) v[e] = tree_load<true>(base + e, slab, M.P);
+  switch (M.P) {
+    case 1: combine_fold<1>(base, slab, v); break;
+    case 2: combine_fold<2>(base, slab, v); break;
+    case 4: combine_fold<4>(base, slab, v); break;
+    case 8: combine_fold<8>(base, slab, v); break;
+    default: combine_fold<16>(base, slab, v); break;
+  }
   fwht128(v, lane);
   float sv[4];
 #pragma unroll
