@@ -157,6 +157,31 @@ __device__ __forceinline__ void bar_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// 16 consecutive TMEM columns of this warp's 32 lanes (one round trip).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Rotated x in the tensor-core layout. Rows are cut into passes of RP rows;
 // pass p holds NMp = min(RP, rows_pad - p*RP) rows (a multiple of 16) and its
 // element (r', k) sits at byte p*RP*K*2 + tk*NMp*32 + ((r'/8)*2 + (k%16)/8)*128
@@ -277,7 +302,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   unsigned char* sX = dsm;                                  // [kTcXS][kTcXStage]
   unsigned char* sA = sX + kTcXS * kTcXStage;               // [kTcAB][kTcAStage]
   float* sEx = reinterpret_cast<float*>(sA + kTcAB * kTcAStage);  // [2][4][128]
-  __shared__ __align__(8) uint64_t xfull[kTcXS], xfree[kTcXS], amma[kTcAB], chunk_done[2];
+  static_assert(kTcAB == kTcXS, "one commit per stage frees its A buffer and its x slot");
+  __shared__ __align__(8) uint64_t xfull[kTcXS], sdone[kTcAB], chunk_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -303,9 +329,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     s_abort = 0;
     for (int i = 0; i < kTcXS; i++) {
       mbar_init(&xfull[i], 1);
-      mbar_init(&xfree[i], 1);
     }
-    for (int i = 0; i < kTcAB; i++) mbar_init(&amma[i], 1);
+    for (int i = 0; i < kTcAB; i++) mbar_init(&sdone[i], 1);
     for (int i = 0; i < 2; i++) mbar_init(&chunk_done[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -402,27 +427,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           tc_fence_after();
           const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * NMf);
           const bool final = c + 1 == M.G;
-          for (int cc = 0; cc < U.NMp; cc += 4) {
-            float v[4];
-            tmem_ld4(cur + (uint32_t)cc, v);
+          // 16 columns (rows of the pass) at a time: cur + the levels the tree
+          // prescribes, parked again or written out
+          for (int cc = 0; cc < U.NMp; cc += 16) {
+            float v[16];
+            tmem_ld16(cur + (uint32_t)cc, v);
             int l = 0;
             for (; l < kTcMaxLevels && ((c >> l) & 1); l++) {
-              float w4[4];
-              tmem_ld4(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), w4);
+              float w[16];
+              tmem_ld16(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), w);
 #pragma unroll
-              for (int e = 0; e < 4; e++) v[e] = w4[e] + v[e];
+              for (int e = 0; e < 16; e++) v[e] = w[e] + v[e];
             }
             if (!final) {
-              tmem_st4(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), v);
+              tmem_st16(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), v);
             } else if (M.P == 1) {
-              tc_rot_out_store(v, n, lane, sEx + (exb & 1) * 512, sv, M.y,
-                               (long long)(U.row0 + cc) * M.N + U.nb * 128 + n, M.N, U.prow - cc, a.act);
-              exb++;
+#pragma unroll
+              for (int q = 0; q < 4; q++) {
+                float v4[4] = {v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]};
+                tc_rot_out_store(v4, n, lane, sEx + (exb & 1) * 512, sv, M.y,
+                                 (long long)(U.row0 + cc + 4 * q) * M.N + U.nb * 128 + n, M.N, U.prow - cc - 4 * q,
+                                 a.act);
+                exb++;
+              }
             } else {
               float* part =
                   M.partial + ((long long)U.pass * M.P + U.gidx) * slab + (long long)cc * M.N + U.nb * 128 + n;
 #pragma unroll
-              for (int e = 0; e < 4; e++)
+              for (int e = 0; e < 16; e++)
                 if (cc + e < U.prow) part[(long long)e * M.N] = v[e];
             }
           }
@@ -455,33 +487,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
         uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
         const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
-        for (int q = 0; q < cnt; q++) {
-          const int i = s0 + q;
-          if (i == cnext) {
-            ci++;
-            gc++;
-            acc = 0;
-            dcol = (uint32_t)((gc & 1) * NMf);
-            cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
-            // the region of chunk gc last held chunk gc-2: it must have been folded
-            if (gc >= 2) bar_sync(kBarFolded + (gc & 1), kFoldedThreads);
-            tc_fence_after();
+        if (cnt == kTcSK && acc && s0 + kTcSK <= cnext) {
+          // the whole stage continues the current chunk: issue it back to back
+          if (lane == 0 && okx && !s_abort) {
+#pragma unroll
+            for (int q = 0; q < kTcSK; q++)
+              umma_f16(tmem + dcol, da + (uint64_t)(q * (4096 >> 4)), db + (uint64_t)(q * db_step), idesc, 1u);
+            if (s0 + kTcSK == cnext) umma_commit(&chunk_done[gc & 1]);
           }
-          if (lane == 0 && okx && !s_abort) umma_f16(tmem + dcol, da, db, idesc, acc);
-          acc = 1;
-          if (lane == 0 && i + 1 == cnext) umma_commit(&chunk_done[gc & 1]);
-          da += 4096 >> 4;
-          db += db_step;
+        } else {
+          for (int q = 0; q < cnt; q++) {
+            const int i = s0 + q;
+            if (i == cnext) {
+              ci++;
+              gc++;
+              acc = 0;
+              dcol = (uint32_t)((gc & 1) * NMf);
+              cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
+              // the region of chunk gc last held chunk gc-2: it must have been folded
+              if (gc >= 2) bar_sync(kBarFolded + (gc & 1), kFoldedThreads);
+              tc_fence_after();
+            }
+            if (lane == 0 && okx && !s_abort) umma_f16(tmem + dcol, da, db, idesc, acc);
+            acc = 1;
+            if (lane == 0 && i + 1 == cnext) umma_commit(&chunk_done[gc & 1]);
+            da += 4096 >> 4;
+            db += db_step;
+          }
         }
         if (lane == 0) {
-          umma_commit(&amma[ab]);
-          umma_commit(&xfree[xs]);
+          umma_commit(&sdone[ab]);  // frees A buffer ab and x slot xs (the same index)
         }
         __syncwarp();
         // release the A buffer of the previous stage once its MMAs are done
         const int r = gs - 1;
         if (r >= 0 && r + kTcAB < total) {
-          if (lane == 0) mbar_wait(&amma[r % kTcAB], (r / kTcAB) & 1, &s_abort, ta.err);
+          if (lane == 0) mbar_wait(&sdone[r % kTcAB], (r / kTcAB) & 1, &s_abort, ta.err);
           __syncwarp();
           bar_arrive(kBarFree + r % kTcAB, kReadyThreads);
         }
@@ -506,7 +547,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
           const int cnt = min(kTcSK, U.nsteps - s0);
           const int xs = gs % kTcXS;
-          if (gs >= kTcXS && !mbar_wait(&xfree[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, 32)) continue;
+          if (gs >= kTcXS && !mbar_wait(&sdone[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, 32)) continue;
           if (s_abort) continue;
           const uint32_t bytes = (uint32_t)(cnt * U.NMp * 32);
           mbar_expect_tx(&xfull[xs], bytes);
