@@ -232,9 +232,16 @@ struct Family {
 
 int row_tile(int rows) { return rows <= 8 ? 0 : rows <= 16 ? 1 : rows <= 32 ? 2 : 3; }
 
-Family pick(int bits, int rows) {
+// Above 32 rows the tensor-core kernel overtakes the decode-rows kernels on
+// large layers (measured on GB300: 5120 x 2*17408 at 64 rows 158 vs 180 us;
+// 5120 x 5120 at 64 rows 45 vs 36 us), so auto picks it there once a call has
+// at least kTcMidWeights weights.
+constexpr long long kTcMidWeights = 64LL << 20;
+
+Family pick(int bits, int rows, long long weights = 0) {
   const tfx::KernelSet& ks = kernels(bits);
-  if (g_variant != 2 && rows <= tfx::kRowsMaxRows) {
+  const bool mid_tc = g_variant == 0 && rows > 32 && weights >= kTcMidWeights;
+  if (g_variant != 2 && rows <= tfx::kRowsMaxRows && !mid_tc) {
     const int i = row_tile(rows);
     if (g_variant == 1) return Family{ks.linear_rows[i], tfx::kRowsTC * tfx::kRowsGW, 1, kRowsCta};
     return Family{ks.linear_warp[i], tfx::kWarpCta, i < 2 ? 2 : 1, kRowsWarp};
@@ -393,7 +400,9 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ra.count = count;
   ra.rows = rows;
   ra.rows_pad = (rows + 15) / 16 * 16;
-  const Family f = pick(bits, rows);
+  long long weights = 0;
+  for (int i = 0; i < count; i++) weights += (long long)K * ws[i]->N;
+  const Family f = pick(bits, rows, weights);
   if (f.rows()) ra.rows_pad = tfx::x_rows_padded(rows);  // whole row tiles, zero-padded
   ra.K = K;
   ra.act = ws[0]->act;

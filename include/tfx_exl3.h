@@ -132,8 +132,9 @@ int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk);
 int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
 
 /* Kernel family for the next calls. 0 = auto: 1..64 rows the warp-granular
- * decode-rows kernel (C FP32 slabs folded by a combine kernel), more rows the
- * tensor-core kernel; 1 = for 1..64 rows the CTA decode-rows kernel whose
+ * decode-rows kernel (C FP32 slabs folded by a combine kernel), except 33..64
+ * rows on calls of at least 64 Mi weights, which go to the tensor-core kernel
+ * like every call above 64 rows; 1 = for 1..64 rows the CTA decode-rows kernel whose
  * split-K partials are summed in-kernel by the last CTA to arrive on each
  * block's counter (the counter resets itself), more rows as auto; 2 = the
  * tensor-core kernel for every row count. All give the same bytes. Initial
