@@ -5,7 +5,8 @@ Workload (decode rows at the 27B shapes): K = 5120, 4-bit trellis codes, 16
 rows of FP16 activations. One step is one q/k/v group call (N = 6144 + 1024 +
 1024: one rotation launch and one linear launch) followed by one single call on
 a 5120 x 5120 weight: the whole hot path (rotation, weight stream, decode, MMA,
-split-K combine with self-resetting counters, output rotation) over one batch.
+split-K combine, output rotation) over one batch. The timed K steps replay from
+one CUDA graph.
 
 Metric: weight-stream GB/s (packed code bytes of every weight the step reads /
 step time), with µs per call alongside. Weights cycle through enough distinct
@@ -73,7 +74,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
@@ -220,7 +221,8 @@ def run_gpu(args):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
 
     # weights: enough distinct copies of the step's four weights to exceed 4x L2
     copies = max(2, -(-4 * L2_BYTES // STEP_WEIGHT_BYTES))
@@ -230,60 +232,57 @@ def run_gpu(args):
         t = torch.from_numpy(codes.view(np.int32)).to(dev)
         su = torch.from_numpy(synth.suh(seed, K, member).view(np.int16)).to(dev)
         sv = torch.from_numpy(synth.svh(seed, N, member).view(np.int16)).to(dev)
-        w = tfx.Weight(t, su, sv, K, N, BITS, tfx.F16)
-        tfx.reserve(w, ROWS, stream)
-        return w
+        return t, su, sv, N
 
     base = [up(1000 + rank, N, m) for m, N in enumerate(QKV)] + [up(1000 + rank, O_N, 3)]
     sets = []
     for c in range(copies):
         ws_c = []
-        for w in base:
-            t = w._keep[0].clone()  # same codes, distinct memory
-            wc = tfx.Weight(t, w._keep[1], w._keep[2], K, w.N, BITS, tfx.F16)
-            tfx.reserve(wc, ROWS, stream)
+        for (t, su, sv, N) in base:
+            wc = tfx.Weight(t.clone(), su, sv, K, N, BITS, tfx.F16)  # same codes, distinct memory
+            tfx.reserve(wc, 128, stream)
             ws_c.append(wc)
         sets.append(ws_c)
     x = torch.from_numpy(synth.activations(1000 + rank, ROWS, K, "f16")).to(dev)
-    ys = [torch.empty((ROWS, n), dtype=torch.float16, device=dev) for n in QKV]
-    yo = torch.empty((ROWS, O_N), dtype=torch.float16, device=dev)
+    # the four outputs are consecutive slices of one buffer: one D2H copy per step
+    y_all = torch.empty(ROWS * (sum(QKV) + O_N), dtype=torch.float16, device=dev)
+    offs = np.cumsum([0] + [ROWS * n for n in QKV + (O_N,)])
+    ys = [y_all[offs[i]:offs[i + 1]].view(ROWS, n) for i, n in enumerate(QKV)]
+    yo = y_all[offs[3]:offs[4]].view(ROWS, O_N)
 
-    def event_pairs(n):
-        # torch creates the CUDA event lazily: record each once so its handle exists
-        out = []
-        for _ in range(n):
-            pr = []
-            for _ in range(2):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                b.record(stream)
-                pr.append((a, b))
-            out.append(pr)
-        return out
-
-    def step(i, marks=None):
+    def step(i, xin=x, rows=ROWS):
         q, k, v, o = sets[i % copies]
-        if marks:
-            tfx.mark_events(*marks[0])
-        tfx.group([q, k, v], x, ROWS, ys, stream)
-        if marks:
-            tfx.mark_events(*marks[1])
-        tfx.linear(o, x, ROWS, yo, stream)
+        tfx.group([q, k, v], xin[:rows], rows, [y[:rows] for y in ys], stream)
+        tfx.linear(o, xin[:rows], rows, yo[:rows], stream)
+
+    def capture(fn, n):
+        """A CUDA graph of fn(0) .. fn(n-1) on the bench stream (the calls allocate nothing)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i)
+        return g
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
 
-    # device-resident timing, with the linear kernels' own events on the launching stream
-    kern_pairs = event_pairs(args.steps)
+    # the timed region: exactly K steps, replayed from one CUDA graph (one
+    # launch per kernel, no host work between them), weights resident in HBM
+    g_steps = capture(step, args.steps)
+    g_steps.replay()  # untimed: first replay after instantiation
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # keep the GPU busy while the sampler starts, so the samples see the load
+        t_end = time.perf_counter() + 0.5
+        while time.perf_counter() < t_end:
+            g_steps.replay()
+            torch.cuda.synchronize()
         barrier(ws)
         torch.cuda.synchronize()
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for i in range(args.steps):
-            step(i, kern_pairs[i])
+        g_steps.replay()
         stop.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
@@ -292,14 +291,42 @@ def run_gpu(args):
     ms_max = reduce_max(ms, ws, dev)
     sec_per_step = ms_max / 1e3 / args.steps
     value = ws * STEP_WEIGHT_BYTES / sec_per_step / 1e9
+    del g_steps
 
-    # dominant kernel: the linear kernel (group launch and single launch)
+    # dominant kernel: the linear kernel of each call (group launch and single
+    # launch), timed with CUDA events recorded by the library around its launch
+    # on the launching stream
+    n_k = 100
+    kern_pairs = []
+    for _ in range(n_k):
+        pr = []
+        for _ in range(2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            b.record(stream)
+            pr.append((a, b))
+        kern_pairs.append(pr)
+    torch.cuda.synchronize()
+
+    def marked_step(i):
+        q, k, v, o = sets[i % copies]
+        tfx.mark_events(*kern_pairs[i][0])
+        tfx.group([q, k, v], x, ROWS, ys, stream)
+        tfx.mark_events(*kern_pairs[i][1])
+        tfx.linear(o, x, ROWS, yo, stream)
+
+    # the GPU first sleeps while the host enqueues every marked call, so the
+    # kernels run back to back and the events see device time only
+    torch.cuda._sleep(int(2e7))
+    for i in range(n_k):
+        marked_step(i)
+    torch.cuda.synchronize()
     kern_ms = [[a.elapsed_time(b) for (a, b) in p] for p in kern_pairs]
     grp_ms = statistics.mean(k[0] for k in kern_ms)
     one_ms = statistics.mean(k[1] for k in kern_ms)
 
     def alg_bytes(Ns):
-        # packed codes + rotated x read + svh + y written (split-K scratch excluded)
+        # packed codes + rotated x read + svh + y written
         return sum(packed_bytes(K, n, BITS) + 2 * ROWS * K + 2 * n + 2 * ROWS * n for n in Ns)
 
     kern_s = (grp_ms + one_ms) / 1e3
@@ -319,61 +346,71 @@ def run_gpu(args):
         if d.get("kernel_source_sha256") == kernel_source_hash():
             traffic = d.get("bytes_per_launch_decode_rows_step")
 
-    # end-to-end: pinned host x -> device, the two calls, y -> pinned host, every step
+    # end to end through the public API: every step copies x from pinned host
+    # memory to the device, runs the two calls and copies the outputs back to
+    # pinned host memory; the K steps replay from one CUDA graph
     xh = x.cpu().pin_memory()
-    yh = [torch.empty((ROWS, n), dtype=torch.float16).pin_memory() for n in QKV + (O_N,)]
+    yh = torch.empty(y_all.numel(), dtype=torch.float16).pin_memory()
     xd = torch.empty_like(x)
-    for i in range(3):
-        xd.copy_(xh, non_blocking=True)
-        step(i)
-    torch.cuda.synchronize()
-    barrier(ws)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
+
+    def e2e_step(i):
         xd.copy_(xh, non_blocking=True)
         q, k, v, o = sets[i % copies]
         tfx.group([q, k, v], xd, ROWS, ys, stream)
         tfx.linear(o, xd, ROWS, yo, stream)
-        for hbuf, dbuf in zip(yh, ys + [yo]):
-            hbuf.copy_(dbuf, non_blocking=True)
+        yh.copy_(y_all, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    g_e2e = capture(e2e_step, args.steps)
+    g_e2e.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g_e2e.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(e0.elapsed_time(e1), ws, dev)
     e2e_value = ws * STEP_WEIGHT_BYTES / (e2e_ms / 1e3 / args.steps) / 1e9
+    del g_e2e
 
-    # per-row-count µs/call (extra detail), same cycling of copies
+    # per-shape µs/call (extra detail): each a CUDA graph of back-to-back calls
+    # cycling through the weight copies
     detail = {}
     if not args.no_detail:
 
         def time_calls(fn, n_calls):
             for i in range(3):
                 fn(i)
+            torch.cuda.synchronize()
+            g = capture(fn, n_calls)
+            g.replay()
+            torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for i in range(n_calls):
-                fn(i)
+            g.replay()
             b.record(stream)
             torch.cuda.synchronize()
             return a.elapsed_time(b) * 1e3 / n_calls
 
+        n_calls = 200
         for rows in (1, 7, 16):
             xr_ = x[:rows]
             detail[f"qkv_group_rows{rows}_us"] = round(time_calls(
                 lambda i, xr_=xr_, rows=rows: tfx.group(sets[i % copies][:3], xr_, rows, [y[:rows] for y in ys], stream),
-                max(20, args.steps)), 3)
+                n_calls), 3)
             detail[f"single_5120_rows{rows}_us"] = round(time_calls(
                 lambda i, xr_=xr_, rows=rows: tfx.linear(sets[i % copies][3], xr_, rows, yo[:rows], stream),
-                max(20, args.steps)), 3)
+                n_calls), 3)
 
         # mid rows on the 5120x5120 weight (same copies, reserved for 128 rows)
         x128 = torch.from_numpy(synth.activations(2000 + rank, 128, K, "f16")).to(dev)
         y128 = torch.empty((128, O_N), dtype=torch.float16, device=dev)
-        for c in range(copies):
-            tfx.reserve(sets[c][3], 128, stream)
         for rows in (64, 128):
             us = time_calls(lambda i, rows=rows: tfx.linear(sets[i % copies][3], x128[:rows], rows, y128[:rows], stream),
-                            max(20, args.steps))
+                            n_calls)
             detail[f"single_5120_rows{rows}_us"] = round(us, 3)
             detail[f"single_5120_rows{rows}_tflops"] = round(2 * rows * K * O_N / us / 1e6, 1)
 
@@ -399,7 +436,7 @@ def run_gpu(args):
         gys = [torch.empty((128, GU), dtype=torch.bfloat16, device=dev) for _ in range(2)]
         for rows in (1, 16, 64, 128):
             us = time_calls(lambda i, rows=rows: tfx.group(gsets[i % gu_copies], xb[:rows], rows,
-                                                           [y[:rows] for y in gys], stream), 20)
+                                                           [y[:rows] for y in gys], stream), 40)
             detail[f"gate_up_rows{rows}_us"] = round(us, 3)
             detail[f"gate_up_rows{rows}_GBps"] = round(gu_bytes / us / 1e3, 1)
             detail[f"gate_up_rows{rows}_tflops"] = round(2 * rows * K * 2 * GU / us / 1e6, 1)
@@ -427,21 +464,21 @@ def run_gpu(args):
                        "K": K, "bits": BITS, "rows": ROWS, "weights_per_step_bytes": STEP_WEIGHT_BYTES,
                        "l2": f"weights cycled through {copies} distinct copies "
                              f"({copies * STEP_WEIGHT_BYTES / 1e6:.0f} MB > 4x L2)",
+                       "timing": "K steps replayed from one CUDA graph, CUDA events on the launching stream",
                        "parallelism": f"replicas x{ws}"},
             "us_per_step": round(sec_per_step * 1e6, 3),
             "detail": detail,
             "roofline": {"bound": "alu", "achieved": round(dec_achieved, 1), "peak": dec_peak,
                          "unit": "G decoded weights/s", "frac": round(dec_achieved / dec_peak, 4), "traffic": traffic,
-                         "kernel": "linear_warp_kernel<4,2,2,3> + tc_combine_kernel (decode rows), "
-                                   "group + single call",
+                         "kernel": "linear_warp_kernel<4,2,2> (decode rows, cluster split-K), group + single call",
                          "peak_source": "derived: 152 SMs x 4 schedulers x 2.07 GHz / 46.5 warp-instructions "
                                         "per 256-weight tile",
                          "hbm": {"achieved": round(hbm_achieved, 1), "peak": peak, "unit": "GB/s",
                                  "frac": round(hbm_achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs"},
                          "kernel_us": {"group": round(grp_ms * 1e3, 3), "single": round(one_ms * 1e3, 3)}},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * 2,
-                    "d2h_bytes_per_step": sum(h.numel() * 2 for h in yh)},
-            "gpu_launches": 6 * args.steps,  # per call: rotation, decode-rows chains, combine
+                    "d2h_bytes_per_step": yh.numel() * 2},
+            "gpu_launches": 4 * args.steps,  # per call: rotation kernel + clustered linear kernel
             "clocks": clocks,
         }
         if cpu is not None:
@@ -464,7 +501,7 @@ def kernel_source_hash() -> str:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")

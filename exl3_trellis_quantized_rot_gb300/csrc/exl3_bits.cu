@@ -50,10 +50,10 @@ KernelSet TFX_CAT(kernels_b, TFX_BITS)() {
       reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 4, TFX_ROWS_PF4, TFX_ROWS_MINB4>);
   k.linear_rows[3] =
       reinterpret_cast<const void*>(&linear_rows_kernel<TFX_BITS, 8, TFX_ROWS_PF8, TFX_ROWS_MINB8>);
-  k.linear_warp[0] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 1, 2, 4>);
-  k.linear_warp[1] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 2, 2, 3>);
-  k.linear_warp[2] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 4, 1, 3>);
-  k.linear_warp[3] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 8, 1, 2>);
+  k.linear_warp[0] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 1, 2>);
+  k.linear_warp[1] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 2, 2>);
+  k.linear_warp[2] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 4, 1>);
+  k.linear_warp[3] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 8, 1>);
   k.linear_tc = reinterpret_cast<const void*>(&linear_tc_kernel<TFX_BITS>);
   k.decode = reinterpret_cast<const void*>(&decode_kernel<TFX_BITS>);
   return k;

@@ -1,6 +1,7 @@
 // Host side of the tfx_exl3 C ABI: validation, plan, scratch reservation,
 // kernel choice and launches. No CPU fallback exists: every step of the
 // layer runs in the kernels of exl3_kernels.cuh.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -30,6 +31,9 @@ namespace tfx {
 // or in core-matrix order (xc_byte) for the tensor-core kernel. One warp per
 // (row, 128-block); x is read once; rows rows..rows_pad-1 are written as zero.
 __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArgs a) {
+  // wait first, then let the linear kernel launch: triggering before the wait
+  // would let the next call's kernels launch (and hold SM resources) while the
+  // previous call still runs, a cascade across a whole graph of calls
   griddep_wait();
   griddep_launch();
   const int lane = threadIdx.x & 31;
@@ -56,8 +60,8 @@ __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArg
 }
 
 __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ CombineArgs ca) {
-  griddep_wait();
   griddep_launch();
+  griddep_wait();
   const LinearArgs& a = ca.la;
   long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -108,9 +112,13 @@ int env_variant() {
   if (!strcmp(v, "mid")) return 2;
   return 0;
 }
+// Programmatic dependent launch is off unless TFX_EXL3_PDL=1: measured on
+// GB300 inside CUDA graphs, letting the clustered linear kernel launch during
+// the rotation kernel made calls slower (5120 x 1024 at 1 row: 13 us against
+// 8.7 us without it), while outside graphs it mostly hides host launch cost.
 int env_pdl() {
   const char* v = getenv("TFX_EXL3_PDL");
-  return !(v && !strcmp(v, "0"));
+  return v && !strcmp(v, "1");
 }
 int g_variant = env_variant();
 thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
@@ -201,19 +209,30 @@ const tfx::KernelSet& kernels(int bits) {
   return ks[bits];
 }
 
-int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void* arg, bool pdl) {
+// Launch with an optional programmatic dependency on the previous kernel of
+// the stream and an optional 1-D cluster of `cluster` CTAs.
+int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void* arg, bool pdl, int cluster = 1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int na = 0;
   if (pdl) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    na++;
   }
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    na++;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   void* args[1] = {arg};
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -227,6 +246,7 @@ struct Family {
   int wpc;   // warps per CTA
   int ncol;  // tile-columns per warp (warp-granular kernel)
   Kind kind;
+  int nr;    // 8-row groups of the decode-rows row tile
   bool rows() const { return kind != kTensor; }
 };
 
@@ -243,10 +263,11 @@ Family pick(int bits, int rows, long long weights = 0) {
   const bool mid_tc = g_variant == 0 && rows > 32 && weights >= kTcMidWeights;
   if (g_variant != 2 && rows <= tfx::kRowsMaxRows && !mid_tc) {
     const int i = row_tile(rows);
-    if (g_variant == 1) return Family{ks.linear_rows[i], tfx::kRowsTC * tfx::kRowsGW, 1, kRowsCta};
-    return Family{ks.linear_warp[i], tfx::kWarpCta, i < 2 ? 2 : 1, kRowsWarp};
+    if (g_variant == 1) return Family{ks.linear_rows[i], tfx::kRowsTC * tfx::kRowsGW, 1, kRowsCta, 1 << i};
+    const int ncol = i < 2 ? 2 : 1;  // must match the instantiations in exl3_bits.cu
+    return Family{ks.linear_warp[i], tfx::warp_cta_warps(ncol), ncol, kRowsWarp, 1 << i};
   }
-  return Family{ks.linear_tc, tfx::kTcThreads / 32, 0, kTensor};
+  return Family{ks.linear_tc, tfx::kTcThreads / 32, 0, kTensor, 0};
 }
 
 // Tensor-core kernel: rows per pass, and chunks per work unit (G). Up to 128
@@ -294,6 +315,127 @@ int set_smem(const void* fn, size_t smem) {
   last_sz[next] = smem;
   next = (next + 1) % 16;
   return 0;
+}
+
+// Shared-memory carveout (percent of the maximum) for a kernel; the call is
+// skipped when the kernel already has that value.
+int set_carveout(const void* fn, int pct) {
+  static thread_local const void* fns[32] = {};
+  static thread_local int vals[32] = {};
+  int slot = -1;
+  for (int i = 0; i < 32; i++) {
+    if (fns[i] == fn) {
+      if (vals[i] == pct) return 0;
+      slot = i;
+      break;
+    }
+    if (!fns[i] && slot < 0) slot = i;
+  }
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(carveout)");
+  if (slot >= 0) {
+    fns[slot] = fn;
+    vals[slot] = pct;
+  }
+  return 0;
+}
+
+// Allow clusters above the portable 8 CTAs for a kernel, once per kernel.
+int allow_big_clusters(const void* fn) {
+  static thread_local const void* done[64] = {};
+  for (int i = 0; i < 64; i++) {
+    if (done[i] == fn) return 0;
+    if (!done[i]) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster size)");
+      done[i] = fn;
+      return 0;
+    }
+  }
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e == cudaSuccess ? 0 : cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster size)");
+}
+
+// cuTensorMapEncodeTiled from the driver the runtime loaded (no link to libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// The trellis of w as a 2-D tensor of uint32 words: x = word within a tile row
+// (the view's N/16 * 8 * bits words), y = tile row (K/16), row pitch = the
+// tile-row stride; boxes of `box_words` x `box_rows`.
+int encode_trellis_map(const tfx_exl3_weight* w, int box_words, int box_rows, CUtensorMap* tm) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return fail(TFX_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)(w->N / 16) * 8 * w->bits, (cuuint64_t)(w->K / 16)};
+  cuuint64_t strides[1] = {(cuuint64_t)w->tile_row_stride * 4};
+  cuuint32_t box[2] = {(cuuint32_t)box_words, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w->trellis), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TFX_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return 0;
+}
+
+// Warp-granular kernel: how the chunk's operands are staged in shared memory,
+// within 40 KB per CTA. The x fragments of the whole chunk form one stage
+// loaded once when they take at most half of it; the trellis words are one
+// box per warp when they fit the rest, else two boxes of H rows in flight
+// (refilled as they are used). When even x does not fit, x and words share
+// H-row boxes, two in flight. Measured on GB300: staging the whole 5120-wide
+// chunk at once (30 KB per CTA at 16 rows) beats smaller boxes that would let
+// all 64 clusters of a q/k/v group be resident at once (25 KB: 68 resident
+// clusters against 54 at 30 KB), because the refills cost more than the
+// second partial wave.
+struct WarpStaging {
+  int H, R, XH, x_whole;
+};
+WarpStaging warp_staging(int K, int bits, int ncol, int nr, long long clusters) {
+  const int C = tfx::chunks_of(K), TK = K / 16;
+  const int nmax = (TK + C - 1) / C;
+  (void)clusters;
+  const int budget = 40 * 1024 - 128;
+  const int wrow = tfx::warp_cta_warps(ncol) * tfx::warp_row_bytes(bits, ncol);  // words of one tile row, all warps
+  const int xrow = nr * 256;                                                       // x of one tile row
+  WarpStaging st{};
+  auto split = [&](int rows_cap) {
+    int h = rows_cap < 1 ? 1 : rows_cap;
+    if (h > nmax) h = nmax;
+    const int nb = (nmax + h - 1) / h;
+    return (nmax + nb - 1) / nb;
+  };
+  if (nmax * xrow <= budget / 2) {
+    st.x_whole = 1;
+    st.XH = nmax;
+    const int left = budget - nmax * xrow;
+    if (nmax * wrow <= left) {
+      st.H = nmax;
+      st.R = 1;
+    } else {
+      st.H = split(left / (2 * wrow));
+      st.R = 2;
+    }
+  } else {
+    st.x_whole = 0;
+    st.H = split(budget / (2 * (wrow + xrow)));
+    st.R = 2;
+    st.XH = st.H;
+  }
+  return st;
 }
 
 // Validation of a call; on success every member is well formed and aligned.
@@ -414,9 +556,6 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ra.rp_tc = tc_rows_per_pass(rows);
   const long long items = (long long)ra.rows_pad * (K / 128);
   int rc = 0;
-  rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
-              pdl);
-  if (rc) return rc;
 
   // one grid over every member's CTAs
   LinearArgs la = {};
@@ -428,6 +567,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   la.passes = (rows + per_pass - 1) / per_pass;
   la.rp = rows < per_pass ? rows : per_pass;
   la.act = ws[0]->act;
+  la.err = sc.err;
   long long ctas = 0;
   int tcG = 0;
   if (!f.rows()) {
@@ -450,12 +590,13 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     m.C = chunks_of(K);
     m.cta_begin = (int)ctas;
     if (f.kind == kRowsWarp) {
-      // one warp per (ncol tile-columns, chunk): C slabs folded by the combine kernel
+      // one CTA per (128-column block, chunk); the C CTAs of a block are one
+      // cluster that folds the chunk sums in distributed shared memory
       m.G = 1;
       m.TC = f.ncol;
-      m.P = m.C;
+      m.P = 1;
       m.arrivals = 0;
-      ctas += (long long)(w->N / 16 / f.ncol) * m.C;
+      ctas += (long long)m.NB * m.C;
     } else if (f.kind == kRowsCta) {
       const int TN = w->N / 16;
       m.G = rows_group(TN, m.C, rows);
@@ -474,9 +615,29 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     m.log2G = __builtin_ctz(m.G);
   }
   la.items = ctas;
-  if (f.kind == kRowsWarp) ctas = (ctas + f.wpc - 1) / f.wpc;  // wpc independent warps per CTA
   if (ctas > 0x7fffffffLL) return fail(TFX_EUNSUPPORTED, "grid of %lld CTAs", ctas);
-  const size_t smem = f.rows() ? 0 : kTcDynSmem;
+  size_t smem = f.rows() ? 0 : kTcDynSmem;
+  if (f.kind == kRowsWarp) {
+    // tensor maps of the members' trellis words and the box shape
+    long long clusters = 0;
+    for (int i = 0; i < count; i++) clusters += ws[i]->N / 128;
+    const WarpStaging stg = warp_staging(K, bits, f.ncol, f.nr, clusters);
+    la.box_rows = stg.H;
+    la.ring_boxes = stg.R;
+    la.x_rows = stg.XH;
+    la.x_whole = stg.x_whole;
+    for (int i = 0; i < count; i++) {
+      rc = encode_trellis_map(ws[i], f.ncol * 8 * bits, stg.H, &la.tm[i]);
+      if (rc) return rc;
+    }
+    smem = (size_t)tfx::warp_smem_bytes(stg.H, stg.R, stg.XH, stg.x_whole, bits, f.ncol, f.nr, rows);
+    // the largest carveout, set once: both operands come through shared memory;
+    // clusters of 16 CTAs (16 chunks) need the non-portable size opt-in
+    rc = set_carveout(f.fn, 100);
+    if (rc) return rc;
+    rc = allow_big_clusters(f.fn);
+    if (rc) return rc;
+  }
   rc = set_smem(f.fn, smem);
   if (rc) return rc;
   TcArgs ta;
@@ -489,13 +650,18 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     const long long S = sm_count();
     ctas = ctas < S ? ctas : S;  // persistent: one CTA per SM at most
   }
+  // everything that can fail on the host is done: enqueue the rotation, then the linear kernel
+  rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
+              pdl);
+  if (rc) return rc;
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && cudaEventRecord(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
-  rc = f.rows() ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl)
+  const int cluster = f.kind == kRowsWarp ? chunks_of(K) : 1;
+  rc = f.rows() ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl, cluster)
                 : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
   if (rc) return rc;
-  if (f.kind == kRowsWarp || f.kind == kTensor) {
+  if (f.kind == kTensor) {
     // members split over P > 1 units: fold their slabs, one warp per (row, block)
     CombineArgs ca = {};
     ca.la = la;

@@ -28,13 +28,20 @@
 //   without changing a bit. The pages fix the determinism (PR #1467, "The
 //   arithmetic": the mid-M kernels keep the linear's K ranges, warp-order sums
 //   and split-order partials), not the tree shape.
-// Split-K combine: each CTA writes the sum of its subtree to a scratch slab,
-//   then one thread publishes it (fence + atomic increment of the 128-column
-//   block's counter). The CTA that sees the last arrival folds the slabs as a
-//   tree, applies the output rotation and svh, stores y and resets the counter
-//   to 0 (PR #1475, "What this changes": the last arriving program resets
-//   counters[pass*NB + nb]). No CTA ever waits on another.
+// Split-K combine, three forms with the same arithmetic:
+//   * decode rows (default): the C CTAs of a 128-column block are one cluster;
+//     each parks its chunk sums in shared memory and, after a cluster barrier,
+//     folds some rows of the block from all C CTAs' shared memory;
+//   * decode rows, `rows` variant: each CTA writes its subtree sum to a scratch
+//     slab and one thread publishes it (fence + atomic increment of the
+//     block's counter); the CTA that sees the last arrival folds the slabs,
+//     rotates back, stores y and resets the counter to 0 (PR #1475, "What this
+//     changes": the last arriving program resets counters[pass*NB + nb]);
+//   * tensor core: units write slabs that a combine kernel folds.
+//   No CTA ever spins on another CTA's progress (cluster barriers are
+//   hardware barriers of co-scheduled CTAs).
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -73,6 +80,13 @@ struct LinearArgs {
   int rp;       // row stride of a partial slab = min(rows, 128)
   int act;      // 0 FP16, 1 BF16
   long long items;  // work items of the warp-granular kernel (all members)
+  int* err;         // device error word of the call
+  int box_rows;     // warp-granular kernel: tile rows per tensor copy of trellis words (H)
+  int ring_boxes;   // warp-granular kernel: trellis copies in flight per warp (R, 1 or 2)
+  int x_rows;       // warp-granular kernel: tile rows per x stage (the whole chunk, or H)
+  int x_whole;      // warp-granular kernel: 1 if one x stage holds the whole chunk
+  CUtensorMap tm[3];  // warp-granular kernel: member m's trellis as a 2-D tensor of uint32
+                      // words (columns of the view x K/16 tile rows), box (NCOL*8*BITS, H)
 };
 
 struct RotArgs {
@@ -99,10 +113,53 @@ __host__ __device__ __forceinline__ long long xf_index(int q, int tk, int lane, 
   return ((long long)q * TK + tk) * 32 + lane;
 }
 
-__host__ __device__ __forceinline__ int chunk_begin(int c, int TK, int C) { return (int)(((long long)c * TK) / C); }
+// log2 of a power of two
+__host__ __device__ __forceinline__ int ilog2_pow2(int C) {
+#ifdef __CUDA_ARCH__
+  return __ffs(C) - 1;
+#else
+  return __builtin_ctz((unsigned)C);
+#endif
+}
+// First tile row of chunk c: floor(c * TK / C), C a power of two.
+__host__ __device__ __forceinline__ int chunk_begin(int c, int TK, int C) {
+  return (int)(((long long)c * TK) >> ilog2_pow2(C));
+}
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// mbarrier and bulk-copy (TMA engine) primitives, CTA scope.
+__device__ __forceinline__ uint32_t s_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s_addr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(s_addr(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(s_addr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(s_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   s_addr(dst)),
+               "l"(src), "r"(bytes), "r"(s_addr(b))
+               : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
 // Balanced binary tree over n values in index order: (v0+v1), (v2+v3), ...
 template <int N>
@@ -402,7 +459,6 @@ __device__ __forceinline__ const Member& pick_member_at(const LinearArgs& a, lon
 }
 __device__ __forceinline__ const Member& pick_member(const LinearArgs& a) { return pick_member_at(a, blockIdx.x); }
 
-constexpr int kWarpCta = 1;  // warps (independent work items) per CTA of the warp-granular kernel
 
 // ---------------------------------------------------------------------------
 // Decode-rows kernel (1..64 rows in row tiles of 8*NR, one pass). One CTA = WPC warps = WPC
@@ -484,7 +540,7 @@ __device__ __forceinline__ void rows_chain(const uint32_t* __restrict__ tp, long
     if (p < n) {
       WF::load(tp + p * wstride, lw, lane, own[p]);
 #pragma unroll
-      for (int q = 0; q < NR; q++) xr[p][q] = __ldg(xp + q * xstride_q + 32 * p);
+      for (int q = 0; q < NR; q++) xr[p][q] = __ldcg(xp + q * xstride_q + 32 * p);
     }
   }
   int tk = 0;
@@ -502,7 +558,7 @@ __device__ __forceinline__ void rows_chain(const uint32_t* __restrict__ tp, long
       if (nx < n) {
         WF::load(tp + nx * wstride, lw, lane, own[p]);
 #pragma unroll
-        for (int q = 0; q < NR; q++) xr[p][q] = __ldg(xp + q * xstride_q + 32 * nx);
+        for (int q = 0; q < NR; q++) xr[p][q] = __ldcg(xp + q * xstride_q + 32 * nx);
       }
       rows_step<BITS, NR>(oc, xc, lw, lane, acc);
     }
@@ -602,105 +658,313 @@ __global__ void __launch_bounds__(kRowsTC * kRowsGW * 32, MINB)
   if (threadIdx.x == 0) M.counters[nb] = 0;
 }
 
-// Warp-granular decode-rows kernel (1..64 rows, one pass): one warp = NCOL
-// adjacent tile-columns x one K chunk, one warp per CTA, so the hardware
-// spreads the work over the SMs in units of one chain (TK/C tiles) and no SM
-// carries a whole extra CTA of work. The trellis words of the first PF tiles
-// are requested before the wait on the rotation kernel (they do not depend on
-// it). The chain runs from zero like every chunk; its FP32 result is slab
-// `chunk` of P = C slabs, and tc_combine_kernel folds each block's C slabs as
-// the chunk tree prescribes (a balanced binary tree in chunk order), rotates
-// back and stores y.
-template <int BITS, int NR, int NCOL, int PF>
-__global__ void __launch_bounds__(32 * kWarpCta) linear_warp_kernel(const __grid_constant__ LinearArgs a) {
-  using WF = WordFetch<BITS>;
-  const int lane = threadIdx.x & 31;
-  const long long item = (long long)blockIdx.x * kWarpCta + (threadIdx.x >> 5);
-  if (item >= a.items) return;
-  const Member& M = pick_member_at(a, item);
-  const int local = (int)(item - M.cta_begin);
-  const int chunk = local % M.C;
-  const int tn0 = (local / M.C) * NCOL;
+// Warp-granular decode-rows kernel (1..64 rows, one pass). A CTA covers one
+// 128-column block for one K chunk: 8/NCOL warps, warp w owning NCOL adjacent
+// tile-columns, each running that chunk's MMA chain for them. The C CTAs of a
+// block (its C chunks) form one thread-block cluster. Both operands are moved
+// by the copy engine into shared memory:
+//   * the warp's trellis words: before anything else, lane 0 asks for the
+//     chain's tile rows as 2-D boxes of H rows x NCOL tiles (one tensor copy
+//     per box) into the warp's own ring of R (1 or 2) boxes, so a whole SM's
+//     share of a small layer is in flight from the first cycles; a finished
+//     box is refilled with the box R further on;
+//   * the rotated x of the chunk (written by the rotation kernel, so read only
+//     after the wait on it): thread 0 bulk-copies the matching H tiles of x
+//     fragments into the CTA's ring of R stages, shared by its warps; a stage
+//     is refilled once every warp has arrived on its `empty` barrier.
+// Split-K combine inside the cluster: every CTA parks its chain sums (rows x
+// 128 FP32) in its own shared memory; after a cluster barrier, the CTA of
+// chunk i folds rows i, i + C, ... : one warp per row reads the C chunk sums
+// of the row from the C CTAs' shared memory (distributed shared memory),
+// adds them as the chunk tree prescribes (a balanced binary tree in chunk
+// order), rotates back (FWHT, 1/sqrt(128)), scales by svh and stores y. A
+// second cluster barrier keeps every CTA's shared memory alive until all
+// reads are done. No scratch, no counters, no second kernel.
+constexpr long long kSpinClocks = 2000000000LL;  // clock cycles before a wait gives up (about 1 s)
+
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// descheduled until it completes or about `ns` nanoseconds pass, so waiting
+// warps leave the issue slots to the warps that decode.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* b, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(s_addr(b)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of the given parity, at most kSpinClocks; false on a timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity) {
+  if (mbar_test(b, parity)) return true;
+  const long long t0 = clock64();
+  uint32_t ns = 32;
+  while (!mbar_test_sleep(b, parity, 20000u)) {
+    if (clock64() - t0 > kSpinClocks) return false;
+    __nanosleep(ns);
+    if (ns < 512) ns *= 2;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          s_addr(dst)),
+      "l"(tm), "r"(x), "r"(y), "r"(s_addr(b))
+      : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 16 bytes at the same shared-memory offset in the CTA of cluster rank `rank`
+__device__ __forceinline__ float4 ld_dsmem_f4(const void* local, int rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(s_addr(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+// Fold the P chunk sums of one row (4 consecutive columns per lane) held by
+// the cluster's CTAs at the same offset, as a balanced tree in chunk order.
+template <int P>
+__device__ __forceinline__ void cluster_fold(const float* local, float (&v)[4]) {
+  float4 s[P];
+#pragma unroll
+  for (int p = 0; p < P; p++) s[p] = ld_dsmem_f4(local, p);
+  float t[4][P];
+#pragma unroll
+  for (int p = 0; p < P; p++) {
+    t[0][p] = s[p].x;
+    t[1][p] = s[p].y;
+    t[2][p] = s[p].z;
+    t[3][p] = s[p].w;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; e++) v[e] = tree_sum<P>(t[e]);
+}
+
+// Rotate one row of a 128-column block back and store it: FWHT over the 128
+// values (4 per lane), x 1/sqrt(128), x svh, round to the output dtype.
+__device__ __forceinline__ void rot_out_row(float (&v)[4], const __half* svh, void* y, long long yo, int act,
+                                            int lane) {
+  fwht128(v, lane);
+  float sv[4];
+#pragma unroll
+  for (int e = 0; e < 4; e++) sv[e] = __half2float(svh[e]);
+#pragma unroll
+  for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
+  uint2 out;
+  if (act == 0) {
+    __half2 o0 = __floats2half2_rn(v[0], v[1]), o1 = __floats2half2_rn(v[2], v[3]);
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(y) + yo) = out;
+  } else {
+    __nv_bfloat162 o0 = __floats2bfloat162_rn(v[0], v[1]), o1 = __floats2bfloat162_rn(v[2], v[3]);
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(y) + yo) = out;
+  }
+}
+
+// Shared memory of the warp-granular kernel: R stages of x (NR row groups x H
+// tiles x 256 bytes) and, per warp, R boxes of H tile rows of NCOL tiles (each
+// padded to 128 bytes); after the chains the same space holds the CTA's chain
+// sums (rows x 128 FP32). Plus 128 bytes of alignment slack.
+__host__ __device__ constexpr int warp_cta_warps(int ncol) { return 8 / ncol; }
+__host__ __device__ constexpr int warp_row_bytes(int bits, int ncol) { return ncol * 32 * bits; }
+__host__ __device__ inline int warp_box_bytes(int H, int bits, int ncol) {
+  return (H * warp_row_bytes(bits, ncol) + 127) & ~127;
+}
+__host__ __device__ inline int warp_x_stage_bytes(int H, int nr) { return nr * H * 256; }
+__host__ __device__ inline int warp_smem_bytes(int H, int R, int XH, int x_whole, int bits, int ncol, int nr,
+                                               int rows) {
+  const int ring = (x_whole ? 1 : R) * warp_x_stage_bytes(XH, nr) + R * warp_cta_warps(ncol) * warp_box_bytes(H, bits, ncol);
+  const int park = rows * 128 * 4;
+  return (ring > park ? ring : park) + 128;
+}
+
+template <int BITS, int NR, int NCOL>
+__global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(const __grid_constant__ LinearArgs a) {
+  constexpr int W = warp_cta_warps(NCOL);
+  constexpr int RB = warp_row_bytes(BITS, NCOL);
+  constexpr int RW = RB / 4;
+  extern __shared__ unsigned char wsm[];
+  __shared__ __align__(8) uint64_t wfull[W][2];
+  __shared__ __align__(8) uint64_t xfull[2], xempty[2];
+  __shared__ int s_dead;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long cta = blockIdx.x;
+  int mi = 0;
+  if (a.count > 1 && cta >= a.m[1].cta_begin) mi = 1;
+  if (a.count > 2 && cta >= a.m[2].cta_begin) mi = 2;
+  const Member& M = a.m[mi];
+  const int local = (int)(cta - M.cta_begin);
+  const int lc = ilog2_pow2(M.C);
+  const int chunk = local & (M.C - 1);  // = this CTA's rank in its cluster
+  const int nb = local >> lc;           // 128-column block
+  const int tn0 = nb * 8 + warp * NCOL;
   const int t0 = chunk_begin(chunk, a.TK, M.C), n = chunk_begin(chunk + 1, a.TK, M.C) - t0;
-  LaneWindow<BITS> lw;
-  lw.init(lane);
-  const long long wstride = M.stride;
-  const uint32_t* tp = M.trellis + (long long)t0 * wstride + (long long)tn0 * (8 * BITS);
-  uint32_t own[PF][NCOL][WF::kOwn];
-#pragma unroll
-  for (int p = 0; p < PF; p++)
-    if (p < n)
-#pragma unroll
-      for (int c = 0; c < NCOL; c++) WF::load(tp + p * wstride + c * (8 * BITS), lw, lane, own[p][c]);
+  const int H = a.box_rows, R = a.ring_boxes, XH = a.x_rows;
+  const bool xw = a.x_whole != 0;
+  const int nbox = (n + H - 1) / H;
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(wsm) + 127) & ~uintptr_t(127));
+  const int XS = warp_x_stage_bytes(XH, NR);
+  const int BB = warp_box_bytes(H, BITS, NCOL);
+  const uint2* xs = reinterpret_cast<const uint2*>(base);
+  uint32_t* ring = reinterpret_cast<uint32_t*>(base + (xw ? 1 : R) * XS + warp * R * BB);
+  // the trellis words are the caller's and no kernel of the layer writes them:
+  // ask for them before waiting on the rotation kernel
+  if (lane == 0) {
+    mbar_init(&wfull[warp][0], 1);
+    mbar_init(&wfull[warp][1], 1);
+    if (warp == 0) {
+      mbar_init(&xfull[0], 1);
+      mbar_init(&xfull[1], 1);
+      mbar_init(&xempty[0], W);
+      mbar_init(&xempty[1], W);
+      s_dead = 0;
+    }
+    fence_mbar_init();
+    for (int b = 0; b < R && b < nbox; b++) {
+      mbar_expect_tx(&wfull[warp][b], (uint32_t)(H * RB));
+      tma_load_2d(ring + b * (BB / 4), &a.tm[mi], tn0 * 8 * BITS, t0 + b * H, &wfull[warp][b]);
+    }
+  }
+  __syncthreads();
+  // no early trigger here: the next call's kernels launch when this one ends
+  // (an early trigger lets them occupy SM resources for the whole kernel)
   griddep_wait();
-  griddep_launch();
-  const long long xsq = 32LL * a.TK;
-  const uint2* xp = M.xf + xf_index(0, t0, lane, a.TK);
-  uint2 xr[PF][NR];
-#pragma unroll
-  for (int p = 0; p < PF; p++)
-    if (p < n)
-#pragma unroll
-      for (int q = 0; q < NR; q++) xr[p][q] = __ldg(xp + q * xsq + 32 * p);
+  // x stage of box b: the chunk's tiles [b*H, min(n, (b+1)*H)) of every row
+  // group q (or, with a whole-chunk stage, all n tiles at once), each one
+  // contiguous run of 256 bytes per tile in the fragment layout
+  auto load_x = [&](int b) {
+    const int rows_b = xw ? n : min(H, n - b * H);
+    const int st = xw ? 0 : (b & (R - 1));
+    mbar_expect_tx(&xfull[st], (uint32_t)(NR * rows_b * 256));
+    for (int q = 0; q < NR; q++)
+      bulk_g2s(base + st * XS + q * XH * 256, M.xf + xf_index(q, t0 + (xw ? 0 : b * H), 0, a.TK),
+               (uint32_t)(rows_b * 256), &xfull[st]);
+  };
+  if (threadIdx.x == 0)
+    for (int b = 0; b < (xw ? 1 : R) && b < nbox; b++) load_x(b);
   float acc[NCOL][NR][4];
 #pragma unroll
   for (int c = 0; c < NCOL; c++)
 #pragma unroll
     for (int q = 0; q < NR; q++) acc[c][q][0] = acc[c][q][1] = acc[c][q][2] = acc[c][q][3] = 0.f;
-  auto step = [&](const uint32_t (&ow)[NCOL][WF::kOwn], const uint2 (&xc)[NR]) {
-#pragma unroll
-    for (int c = 0; c < NCOL; c++) {
-      uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
-      WF::gather(ow[c], lw, lane, raw);
-      lw.align(raw, win);
-      decode8<BITS>(win, af);
-#pragma unroll
-      for (int q = 0; q < NR; q++) mma16816(acc[c][q], af, xc[q].x, xc[q].y);
+  LaneWindow<BITS> lw;
+  lw.init(lane);
+  bool alive = true;
+  for (int b = 0; b < nbox && alive; b++) {
+    const int st = b & (R - 1);
+    const uint32_t par = (uint32_t)(b / R) & 1u;
+    bool ok = mbar_wait_bounded(&wfull[warp][st], par);
+    if (xw ? b == 0 : true) ok = ok && mbar_wait_bounded(&xfull[xw ? 0 : st], xw ? 0u : par);
+    if (!__all_sync(0xffffffffu, ok)) {
+      alive = false;
+      break;
     }
-  };
-  int tk = 0;
-  for (; tk + PF <= n; tk += PF) {
+    const uint32_t* wr = ring + st * (BB / 4);
+    const uint2* xr = xw ? xs + lane + b * H * 32 : xs + st * (XS / 8) + lane;
+    const int rows_b = min(H, n - b * H);
+#pragma unroll 2
+    for (int r = 0; r < rows_b; r++) {
+      const uint32_t* rr = wr + r * RW;
+      uint32_t raw[NCOL][Geo<BITS>::kRaw];
 #pragma unroll
-    for (int p = 0; p < PF; p++) {
-      uint32_t oc[NCOL][WF::kOwn];
+      for (int c = 0; c < NCOL; c++) {
+        raw[c][0] = rr[c * 8 * BITS + lw.i0];
+        raw[c][1] = rr[c * 8 * BITS + lw.i1];
+        if constexpr (Geo<BITS>::kRaw > 2) raw[c][2] = rr[c * 8 * BITS + lw.i2];
+      }
       uint2 xc[NR];
 #pragma unroll
-      for (int c = 0; c < NCOL; c++)
+      for (int q = 0; q < NR; q++) xc[q] = xr[(q * XH + r) * 32];
 #pragma unroll
-        for (int i = 0; i < WF::kOwn; i++) oc[c][i] = own[p][c][i];
+      for (int c = 0; c < NCOL; c++) {
+        uint32_t win[Geo<BITS>::kNorm + 1], af[4];
+        lw.align(raw[c], win);
+        decode8<BITS>(win, af);
 #pragma unroll
-      for (int q = 0; q < NR; q++) xc[q] = xr[p][q];
-      const int nx = tk + p + PF;
-      if (nx < n) {
-#pragma unroll
-        for (int c = 0; c < NCOL; c++) WF::load(tp + nx * wstride + c * (8 * BITS), lw, lane, own[p][c]);
-#pragma unroll
-        for (int q = 0; q < NR; q++) xr[p][q] = __ldg(xp + q * xsq + 32 * nx);
+        for (int q = 0; q < NR; q++) mma16816(acc[c][q], af, xc[q].x, xc[q].y);
       }
-      step(oc, xc);
+    }
+    if (b + R < nbox) {
+      // hand the box back: this warp's words to its own next copy, the x
+      // stage to thread 0 once every warp has arrived
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_expect_tx(&wfull[warp][st], (uint32_t)(H * RB));
+        tma_load_2d(ring + st * (BB / 4), &a.tm[mi], tn0 * 8 * BITS, t0 + (b + R) * H, &wfull[warp][st]);
+        if (!xw) {
+          mbar_arrive(&xempty[st]);
+          if (warp == 0) {
+            if (mbar_wait_bounded(&xempty[st], par))
+              load_x(b + R);
+            else
+              s_dead = 1;
+          }
+        }
+      }
     }
   }
-#pragma unroll
-  for (int p = 0; p < PF; p++)
-    if (tk + p < n) step(own[p], xr[p]);
-  // slab `chunk`: lane (g, t) holds (row 8q + 2t | +1, column g | g + 8) of tile-column tn0 + c
-  const int g = lane >> 2, t = lane & 3;
-  float* part = M.partial + (long long)chunk * a.rp * M.N + (long long)tn0 * 16;
-#pragma unroll
-  for (int c = 0; c < NCOL; c++)
-#pragma unroll
-    for (int q = 0; q < NR; q++) {
-      const int r0 = 8 * q + 2 * t;
-      float* pc = part + c * 16 + g;
-      if (r0 < a.rows) {
-        pc[(long long)r0 * M.N] = acc[c][q][0];
-        pc[(long long)r0 * M.N + 8] = acc[c][q][2];
-      }
-      if (r0 + 1 < a.rows) {
-        pc[(long long)(r0 + 1) * M.N] = acc[c][q][1];
-        pc[(long long)(r0 + 1) * M.N + 8] = acc[c][q][3];
-      }
+  if (!alive && lane == 0) s_dead = 1;
+  __syncthreads();
+  const bool dead = s_dead != 0;
+  if (dead) {
+    // a copy never completed: report it and give copies still in flight time
+    // to land in this CTA's shared memory; the cluster still meets at both
+    // barriers, and nothing is written
+    if (threadIdx.x == 0) atomicExch(a.err, 3);
+    const long long w0 = clock64();
+    while (clock64() - w0 < 2000000) {
     }
+  }
+  // park the chain sums: park[r][128] FP32, lane (g, t) holds (row 8q + 2t | +1,
+  // column g | g + 8) of tile-column warp*NCOL + c
+  float* park = reinterpret_cast<float*>(base);
+  {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int c = 0; c < NCOL; c++)
+#pragma unroll
+      for (int q = 0; q < NR; q++) {
+        const int r0 = 8 * q + 2 * t;
+        float* pc = park + (warp * NCOL + c) * 16 + g;
+        if (r0 < a.rows) {
+          pc[r0 * 128] = acc[c][q][0];
+          pc[r0 * 128 + 8] = acc[c][q][2];
+        }
+        if (r0 + 1 < a.rows) {
+          pc[(r0 + 1) * 128] = acc[c][q][1];
+          pc[(r0 + 1) * 128 + 8] = acc[c][q][3];
+        }
+      }
+  }
+  cluster_sync();
+  // rows chunk, chunk + C, ... of this block: one warp per row
+  for (int r = chunk + warp * M.C; r < a.rows && !dead; r += W * M.C) {
+    float v[4];
+    const float* src = park + r * 128 + 4 * lane;
+    switch (M.C) {
+      case 1: cluster_fold<1>(src, v); break;
+      case 2: cluster_fold<2>(src, v); break;
+      case 4: cluster_fold<4>(src, v); break;
+      case 8: cluster_fold<8>(src, v); break;
+      default: cluster_fold<16>(src, v); break;
+    }
+    rot_out_row(v, M.svh + nb * 128 + 4 * lane, M.y, (long long)r * M.N + nb * 128 + 4 * lane, a.act, lane);
+  }
+  cluster_sync();
 }
 
 // Debug: decode every tile to W[k][n] (FP16). One warp per tile.

@@ -132,7 +132,8 @@ int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk);
 int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
 
 /* Kernel family for the next calls. 0 = auto: 1..64 rows the warp-granular
- * decode-rows kernel (C FP32 slabs folded by a combine kernel), except 33..64
+ * decode-rows kernel (one cluster of C CTAs per 128-column block folds the C
+ * chunk sums in distributed shared memory), except 33..64
  * rows on calls of at least 64 Mi weights, which go to the tensor-core kernel
  * like every call above 64 rows; 1 = for 1..64 rows the CTA decode-rows kernel whose
  * split-K partials are summed in-kernel by the last CTA to arrive on each
@@ -142,7 +143,7 @@ int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
 int tfx_exl3_set_variant(int variant);
 
 /* Programmatic dependent launch on (1) or off (0); initial value from
- * TFX_EXL3_PDL (default on). Returns the previous value. */
+ * TFX_EXL3_PDL=1 (default off). Returns the previous value. */
 int tfx_exl3_set_pdl(int on);
 
 /* Test hook: replace the allocator and memset used by reserve/release so the
