@@ -110,6 +110,7 @@ int env_variant() {
   if (!v) return 0;
   if (!strcmp(v, "rows")) return 1;
   if (!strcmp(v, "mid")) return 2;
+  if (!strcmp(v, "warp")) return 3;
   return 0;
 }
 // Programmatic dependent launch is off unless TFX_EXL3_PDL=1: measured on
@@ -247,27 +248,35 @@ struct Family {
   int ncol;  // tile-columns per warp (warp-granular kernel)
   Kind kind;
   int nr;    // 8-row groups of the decode-rows row tile
-  bool rows() const { return kind != kTensor; }
+  // decode-rows families: x in m16n8k16 fragment order, one pass
+  bool rows() const { return kind == kRowsCta || kind == kRowsWarp; }
 };
 
 int row_tile(int rows) { return rows <= 8 ? 0 : rows <= 16 ? 1 : rows <= 32 ? 2 : 3; }
 
-// Above 32 rows the tensor-core kernel overtakes the decode-rows kernels on
-// large layers (measured on GB300: 5120 x 2*17408 at 64 rows 158 vs 180 us;
-// 5120 x 5120 at 64 rows 45 vs 36 us), so auto picks it there once a call has
-// at least kTcMidWeights weights.
+// Kernel choice. auto: up to 64 rows the warp-granular decode-rows kernel,
+// except 33..64 rows on calls of at least kTcMidWeights weights, which go to
+// the persistent tensor-core kernel like every call above 64 rows (measured on
+// GB300: 5120 x 2*17408 at 64 rows 155 us against 180 us for the decode-rows
+// kernel). The other variants force a family where it serves the row count
+// (all give the same bytes).
 constexpr long long kTcMidWeights = 64LL << 20;
 
 Family pick(int bits, int rows, long long weights = 0) {
   const tfx::KernelSet& ks = kernels(bits);
-  const bool mid_tc = g_variant == 0 && rows > 32 && weights >= kTcMidWeights;
-  if (g_variant != 2 && rows <= tfx::kRowsMaxRows && !mid_tc) {
-    const int i = row_tile(rows);
-    if (g_variant == 1) return Family{ks.linear_rows[i], tfx::kRowsTC * tfx::kRowsGW, 1, kRowsCta, 1 << i};
-    const int ncol = i < 2 ? 2 : 1;  // must match the instantiations in exl3_bits.cu
-    return Family{ks.linear_warp[i], tfx::warp_cta_warps(ncol), ncol, kRowsWarp, 1 << i};
+  const int i = rows <= tfx::kRowsMaxRows ? row_tile(rows) : 0;
+  const int ncol = i < 2 ? 2 : 1;  // must match the instantiations in exl3_bits.cu
+  const Family warpk{ks.linear_warp[i], tfx::warp_cta_warps(ncol), ncol, kRowsWarp, 1 << i};
+  const Family rowsk{ks.linear_rows[i], tfx::kRowsTC * tfx::kRowsGW, 1, kRowsCta, 1 << i};
+  const Family tc{ks.linear_tc, tfx::kTcThreads / 32, 0, kTensor, 0};
+  switch (g_variant) {
+    case 1: return rows <= tfx::kRowsMaxRows ? rowsk : tc;
+    case 2: return tc;
+    case 3: return rows <= tfx::kRowsMaxRows ? warpk : tc;
+    default:
+      if (rows <= 32 || (rows <= tfx::kRowsMaxRows && weights < kTcMidWeights)) return warpk;
+      return tc;
   }
-  return Family{ks.linear_tc, tfx::kTcThreads / 32, 0, kTensor, 0};
 }
 
 // Tensor-core kernel: rows per pass, and chunks per work unit (G). Up to 128
@@ -553,7 +562,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     ra.xf[i] = sc.xf[i];
   }
   ra.layout = f.rows() ? 0 : 1;
-  ra.rp_tc = tc_rows_per_pass(rows);
+  ra.rp_tc = tc_rows_per_pass(rows);  // 128 for every call the clustered kernel serves
   const long long items = (long long)ra.rows_pad * (K / 128);
   int rc = 0;
 
@@ -563,14 +572,14 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   la.K = K;
   la.TK = K / 16;
   la.rows = rows;
-  const int per_pass = f.rows() ? kRowsPerPass : tc_rows_per_pass(rows);
+  const int per_pass = f.kind == kTensor ? tc_rows_per_pass(rows) : kRowsPerPass;
   la.passes = (rows + per_pass - 1) / per_pass;
   la.rp = rows < per_pass ? rows : per_pass;
   la.act = ws[0]->act;
   la.err = sc.err;
   long long ctas = 0;
   int tcG = 0;
-  if (!f.rows()) {
+  if (f.kind == kTensor) {
     long long blocks = 0;
     for (int i = 0; i < count; i++) blocks += ws[i]->N / 128;
     tcG = tc_group(blocks, rows, chunks_of(K), K / 16);
@@ -616,7 +625,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   }
   la.items = ctas;
   if (ctas > 0x7fffffffLL) return fail(TFX_EUNSUPPORTED, "grid of %lld CTAs", ctas);
-  size_t smem = f.rows() ? 0 : kTcDynSmem;
+  size_t smem = f.kind == kTensor ? kTcDynSmem : 0;
   if (f.kind == kRowsWarp) {
     // tensor maps of the members' trellis words and the box shape
     long long clusters = 0;
@@ -646,7 +655,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ta.RP = per_pass;
   ta.NMf = per_pass < ra.rows_pad ? per_pass : ra.rows_pad;
   ta.err = sc.err;
-  if (!f.rows()) {
+  if (f.kind == kTensor) {
     const long long S = sm_count();
     ctas = ctas < S ? ctas : S;  // persistent: one CTA per SM at most
   }
@@ -658,8 +667,8 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   g_ev_before = g_ev_after = nullptr;
   if (eb && cudaEventRecord(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
   const int cluster = f.kind == kRowsWarp ? chunks_of(K) : 1;
-  rc = f.rows() ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl, cluster)
-                : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
+  rc = f.kind != kTensor ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl, cluster)
+                         : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
   if (rc) return rc;
   if (f.kind == kTensor) {
     // members split over P > 1 units: fold their slabs, one warp per (row, block)
@@ -790,7 +799,7 @@ int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets) 
 
 int tfx_exl3_set_variant(int variant) {
   const int old = g_variant;
-  if (variant >= 0 && variant <= 2) g_variant = variant;
+  if (variant >= 0 && variant <= 3) g_variant = variant;
   return old;
 }
 

@@ -152,6 +152,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a phase (test_wait never suspends the thread, unlike try_wait).
+__device__ __forceinline__ bool mbar_poll(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(s_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    s_addr(dst)),
@@ -695,16 +705,16 @@ __device__ __forceinline__ bool mbar_test_sleep(uint64_t* b, uint32_t parity, ui
   return ok != 0;
 }
 
-// Wait for the phase of the given parity, at most kSpinClocks; false on a timeout.
+// Wait for the phase of the given parity, at most kSpinClocks; false on a
+// timeout. The wait spins on the non-blocking test: measured on GB300, a
+// try_wait that finds the phase incomplete suspends the thread for a fixed
+// slice (about half a microsecond) rather than until the phase completes,
+// which made every producer/consumer hand-off cost that much.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity) {
-  if (mbar_test(b, parity)) return true;
+  if (mbar_poll(b, parity)) return true;
   const long long t0 = clock64();
-  uint32_t ns = 32;
-  while (!mbar_test_sleep(b, parity, 20000u)) {
+  while (!mbar_poll(b, parity))
     if (clock64() - t0 > kSpinClocks) return false;
-    __nanosleep(ns);
-    if (ns < 512) ns *= 2;
-  }
   return true;
 }
 

@@ -59,15 +59,16 @@ constexpr int kReadyThreads = (kTcDecodeWarps + 1) * 32;
 constexpr int kFoldedThreads = 5 * 32;
 
 // Wait for the phase of the given parity to complete, at most kTcSpin cycles.
-// A completed phase costs one try_wait; otherwise the thread polls, sleeping
-// sleep_ns between polls so that waiting warps leave the issue slots of their
-// scheduler to the warps doing work.
+// The thread polls with the non-blocking test (a try_wait on an incomplete
+// phase suspends the thread for a fixed slice instead of until completion),
+// sleeping sleep_ns between polls so that waiting warps leave the issue slots
+// of their scheduler to the warps doing work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
                                           int sleep_ns = 0) {
   if (*abort_flag) return false;
-  if (mbar_test(b, parity)) return true;
+  if (mbar_poll(b, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_test(b, parity)) {
+  while (!mbar_poll(b, parity)) {
     if (*abort_flag) return false;
     if (sleep_ns) __nanosleep(sleep_ns);
     if (clock64() - t0 > kTcSpin) {

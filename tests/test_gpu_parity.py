@@ -98,7 +98,7 @@ def test_group_planted_controls_go_red(qkv):
 @pytest.mark.parametrize("variant", [tfx.VARIANT_ROWS, tfx.VARIANT_AUTO])
 def test_repeated_calls_need_no_memset(variant):
     # VARIANT_ROWS: every block goes through the in-kernel arrival counters (8 splits);
-    # VARIANT_AUTO: C slabs folded by the combine kernel
+    # VARIANT_AUTO: the cluster of a block folds its chunk sums in shared memory
     hw, w = make(4, 5120, 1024, 4)
     x64, x = x_of(4, 16, 5120)
     tfx.set_variant(variant)
@@ -164,7 +164,7 @@ def test_variants_and_row_counts_byte_identical(K, N, act):
     ref = tfx.linear(w, x)  # 128 rows: mid kernel, NR = 16
     try:
         for rows in (1, 7, 16, 17, 24, 32, 33, 48, 49, 64, 100, 128):
-            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID):
+            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP):
                 tfx.set_variant(var)
                 y = tfx.linear(w, x[:rows])
                 assert same_bytes(y, ref[:rows]), (rows, var)
@@ -266,7 +266,7 @@ def test_nan_and_inf_reach_their_rows_only():
     xb[2, 5] = float("nan")
     xb[3, 700] = float("inf")
     xb[5, 1] = float("-inf")
-    for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID):
+    for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP):
         tfx.set_variant(var)
         try:
             y = tfx.linear(w, xb)
