@@ -315,12 +315,12 @@ def run_gpu(args):
         tfx.mark_events(*kern_pairs[i][1])
         tfx.linear(o, x, ROWS, yo, stream)
 
-    # the GPU first sleeps while the host enqueues every marked call, so the
-    # kernels run back to back and the events see device time only
-    torch.cuda._sleep(int(2e7))
-    for i in range(n_k):
-        marked_step(i)
+    # captured like the timed region (the library records the events as
+    # external event-record nodes), so the events see device time only
+    g_marked = capture(marked_step, n_k)
+    g_marked.replay()
     torch.cuda.synchronize()
+    del g_marked
     kern_ms = [[a.elapsed_time(b) for (a, b) in p] for p in kern_pairs]
     grp_ms = statistics.mean(k[0] for k in kern_ms)
     one_ms = statistics.mean(k[1] for k in kern_ms)
@@ -441,6 +441,58 @@ def run_gpu(args):
             detail[f"gate_up_rows{rows}_GBps"] = round(gu_bytes / us / 1e3, 1)
             detail[f"gate_up_rows{rows}_tflops"] = round(2 * rows * K * 2 * GU / us / 1e6, 1)
         del gsets
+
+        # bit-width sweep: 5120 x 5120 at 1..8 bits, rows 1 and 64, packed bytes per second
+        for bits in range(1, 9):
+            wb = packed_bytes(K, O_N, bits)
+            ncop = max(2, -(-4 * L2_BYTES // wb))
+            codes = torch.from_numpy(synth.codes(5000 + bits, K, O_N, bits).view(np.int32)).to(dev)
+            su = torch.from_numpy(synth.suh(5000 + bits, K).view(np.int16)).to(dev)
+            sv = torch.from_numpy(synth.svh(5000 + bits, O_N).view(np.int16)).to(dev)
+            bws = []
+            for c in range(ncop):
+                wc = tfx.Weight(codes.clone() if c else codes, su, sv, K, O_N, bits, tfx.F16)
+                tfx.reserve(wc, 64, stream)
+                bws.append(wc)
+            for rows in (1, 64):
+                us = time_calls(lambda i, rows=rows: tfx.linear(bws[i % ncop], x128[:rows], rows, y128[:rows], stream),
+                                n_calls)
+                detail[f"bits{bits}_5120_rows{rows}_us"] = round(us, 3)
+                detail[f"bits{bits}_5120_rows{rows}_GBps"] = round(wb / us / 1e3, 1)
+            del bws, codes
+
+        # LM head, 6-bit, K = 5120, N = 248,320: the full head, the view of its first
+        # 98,304 columns, and 64-block views (the last 64 blocks, and distinct 64-block
+        # views of the same head cycled so that every call streams from HBM)
+        HN, HB = 248320, 6
+        hcodes = torch.from_numpy(synth.codes(6000, K, HN, HB).view(np.int32)).to(dev)
+        hsu = torch.from_numpy(synth.suh(6000, K).view(np.int16)).to(dev)
+        hsv = torch.from_numpy(synth.svh(6000, HN).view(np.int16)).to(dev)
+        head = tfx.Weight(hcodes, hsu, hsv, K, HN, HB, tfx.F16)
+        tfx.reserve(head, 16, stream)
+        first = tfx.columns(head, 0, 98304)
+        tfx.reserve(first, 16, stream)
+        tails = []
+        for j in range(8):
+            tv = tfx.columns(head, 240128 - j * 8192 * 3, 8192)
+            tfx.reserve(tv, 16, stream)
+            tails.append(tv)
+        yh_ = torch.empty((16, HN), dtype=torch.float16, device=dev)
+        yf_ = torch.empty((16, 98304), dtype=torch.float16, device=dev)
+        yt_ = torch.empty((16, 8192), dtype=torch.float16, device=dev)
+        for rows in (1, 8, 16):
+            for name, fn, nbytes in (
+                    ("full", lambda i, rows=rows: tfx.linear(head, x[:rows], rows, yh_[:rows], stream),
+                     packed_bytes(K, HN, HB)),
+                    ("first98304", lambda i, rows=rows: tfx.linear(first, x[:rows], rows, yf_[:rows], stream),
+                     packed_bytes(K, 98304, HB)),
+                    ("last64blocks", lambda i, rows=rows: tfx.linear(tails[i % len(tails)], x[:rows], rows,
+                                                                     yt_[:rows], stream),
+                     packed_bytes(K, 8192, HB))):
+                us = time_calls(fn, 20)
+                detail[f"lm_head_{name}_rows{rows}_us"] = round(us, 3)
+                detail[f"lm_head_{name}_rows{rows}_GBps"] = round(nbytes / us / 1e3, 1)
+        del head, first, tails, hcodes
         gate = tfx.Weight(gbase[0][0], gbase[0][1], gbase[0][2], K, GU, BITS, tfx.BF16)
         tfx.reserve(gate, 4096, stream)
         x4k = torch.from_numpy(synth.activations(4000 + rank, 4096, K, "bf16").view(np.int16)).to(dev).view(torch.bfloat16)

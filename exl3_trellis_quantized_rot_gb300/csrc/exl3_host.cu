@@ -447,6 +447,16 @@ WarpStaging warp_staging(int K, int bits, int ncol, int nr, long long clusters) 
   return st;
 }
 
+// Record a measurement event on `s`; inside a stream capture it becomes an
+// event-record node of the graph (external record), so that the event can be
+// timed when the graph is replayed.
+cudaError_t record_event(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return cudaGetLastError();
+  if (st == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  return cudaEventRecord(e, s);
+}
+
 // Validation of a call; on success every member is well formed and aligned.
 int validate_call(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[]) {
   if (count < 1 || count > 3) return fail(TFX_EINVAL, "group count %d outside 1..3", count);
@@ -665,7 +675,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   if (rc) return rc;
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
-  if (eb && cudaEventRecord(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
+  if (eb && record_event(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
   const int cluster = f.kind == kRowsWarp ? chunks_of(K) : 1;
   rc = f.kind != kTensor ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl, cluster)
                          : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
@@ -686,7 +696,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
       if (rc) return rc;
     }
   }
-  if (ea && cudaEventRecord(ea, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
+  if (ea && record_event(ea, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
   return 0;
 }
 

@@ -166,7 +166,9 @@ int tfx_exl3_debug_error(const tfx_exl3_weight* w, int* device_error);
 
 /* Measurement hook: the next linear/group call on this thread records
  * `before` just before its linear-kernel launch and `after` just after it,
- * on the call's stream, then forgets both. Either may be NULL. */
+ * on the call's stream, then forgets both. Either may be NULL. Inside a
+ * stream capture the records become external event-record nodes, so the
+ * events can be timed when the graph is replayed. */
 int tfx_exl3_debug_mark_events(cudaEvent_t before, cudaEvent_t after);
 
 const char* tfx_exl3_last_error(void);
