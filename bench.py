@@ -542,6 +542,49 @@ def run_gpu(args):
     return 0
 
 
+def run_case(args):
+    """A few calls of one workload on cuda:0 and nothing else (the command the
+    ncu captures under profiles/ run): 'qkv_group_rows16' (q/k/v group,
+    K = 5120, 4-bit, 16 rows), 'single_5120_rows16' (5120 x 5120, 4-bit, 16
+    rows) or 'lm_head_rows1' (5120 x 248,320, 6-bit, 1 row)."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import exl3_trellis_quantized_rot_gb300 as tfx
+    import synth
+    dev = torch.device("cuda", 0)
+
+    def weight(seed, N, bits, member=0, copies=1):
+        codes = torch.from_numpy(synth.codes(seed, K, N, bits, member).view(np.int32)).to(dev)
+        su = torch.from_numpy(synth.suh(seed, K, member).view(np.int16)).to(dev)
+        sv = torch.from_numpy(synth.svh(seed, N, member).view(np.int16)).to(dev)
+        out = []
+        for c in range(copies):
+            w = tfx.Weight(codes.clone() if c else codes, su, sv, K, N, bits, tfx.F16)
+            tfx.reserve(w, 16)
+            out.append(w)
+        return out
+
+    x = torch.from_numpy(synth.activations(7, 16, K, "f16")).to(dev)
+    if args.case == "qkv_group_rows16":
+        ms = [weight(7, n, BITS, m, copies=6) for m, n in enumerate(QKV)]
+        for i in range(20):
+            ys = tfx.group([ms[0][i % 6], ms[1][i % 6], ms[2][i % 6]], x)
+    elif args.case == "single_5120_rows16":
+        ws_ = weight(7, O_N, BITS, copies=8)
+        for i in range(20):
+            ys = [tfx.linear(ws_[i % 8], x)]
+    else:
+        head = weight(6000, 248320, 6)[0]
+        for i in range(4):
+            ys = [tfx.linear(head, x[:1])]
+    torch.cuda.synchronize()
+    print(args.case, "ok", float(ys[0].float().abs().mean()))
+    return 0
+
+
 def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -558,9 +601,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-detail", action="store_true", help="skip the per-row-count detail timings")
+    ap.add_argument("--case", choices=["qkv_group_rows16", "single_5120_rows16", "lm_head_rows1"],
+                    help="run a few calls of one workload and exit (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.case:
+        return run_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
