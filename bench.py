@@ -546,7 +546,8 @@ def run_case(args):
     """A few calls of one workload on cuda:0 and nothing else (the command the
     ncu captures under profiles/ run): 'qkv_group_rows16' (q/k/v group,
     K = 5120, 4-bit, 16 rows), 'single_5120_rows16' (5120 x 5120, 4-bit, 16
-    rows) or 'lm_head_rows1' (5120 x 248,320, 6-bit, 1 row)."""
+    rows), 'lm_head_rows1' (5120 x 248,320, 6-bit, 1 row) or 'gate_rows128'
+    (5120 x 17408, 4-bit, 128 rows: the tensor-core kernel)."""
     import numpy as np
     import torch
 
@@ -567,15 +568,21 @@ def run_case(args):
             out.append(w)
         return out
 
-    x = torch.from_numpy(synth.activations(7, 16, K, "f16")).to(dev)
-    if args.case == "qkv_group_rows16":
+    x = torch.from_numpy(synth.activations(7, 128, K, "f16")).to(dev)
+    if args.case == "gate_rows128":
+        ws_ = weight(8, 17408, BITS, copies=3)
+        for w in ws_:
+            tfx.reserve(w, 128)
+        for i in range(6):
+            ys = [tfx.linear(ws_[i % 3], x)]
+    elif args.case == "qkv_group_rows16":
         ms = [weight(7, n, BITS, m, copies=6) for m, n in enumerate(QKV)]
         for i in range(20):
-            ys = tfx.group([ms[0][i % 6], ms[1][i % 6], ms[2][i % 6]], x)
+            ys = tfx.group([ms[0][i % 6], ms[1][i % 6], ms[2][i % 6]], x[:16])
     elif args.case == "single_5120_rows16":
         ws_ = weight(7, O_N, BITS, copies=8)
         for i in range(20):
-            ys = [tfx.linear(ws_[i % 8], x)]
+            ys = [tfx.linear(ws_[i % 8], x[:16])]
     else:
         head = weight(6000, 248320, 6)[0]
         for i in range(4):
@@ -601,7 +608,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-detail", action="store_true", help="skip the per-row-count detail timings")
-    ap.add_argument("--case", choices=["qkv_group_rows16", "single_5120_rows16", "lm_head_rows1"],
+    ap.add_argument("--case", choices=["qkv_group_rows16", "single_5120_rows16", "lm_head_rows1", "gate_rows128"],
                     help="run a few calls of one workload and exit (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
