@@ -254,6 +254,11 @@ struct Family {
 
 int row_tile(int rows) { return rows <= 8 ? 0 : rows <= 16 ? 1 : rows <= 32 ? 2 : 3; }
 
+// Calls of at most this many rows skip the rotation kernel: the decode-rows
+// kernel rotates each CTA's chunk of x itself.
+constexpr int kFuseRotRows = 4;
+constexpr long long kFuseRotWeights = 64LL << 20;
+
 // Kernel choice. auto: up to 64 rows the warp-granular decode-rows kernel,
 // except 33..64 rows on calls of at least kTcMidWeights weights, which go to
 // the persistent tensor-core kernel like every call above 64 rows (measured on
@@ -600,6 +605,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     m.trellis = w->trellis;
     m.stride = w->tile_row_stride;
     m.svh = reinterpret_cast<const __half*>(w->svh);
+    m.suh = reinterpret_cast<const __half*>(w->suh);
     m.xf = sc.xf[i];
     m.y = ys[i];
     m.partial = sc.partial[i];
@@ -645,6 +651,14 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     la.ring_boxes = stg.R;
     la.x_rows = stg.XH;
     la.x_whole = stg.x_whole;
+    // up to kFuseRotRows rows, on calls of fewer than kFuseRotWeights weights,
+    // each CTA rotates its chunk of x itself: a few warp-items per CTA, cheaper
+    // than the rotation kernel and its launch on the critical path of a
+    // latency-bound call (measured on GB300: 5120 x 5120 at 1 row 13.9 -> 12.8
+    // us); on large calls the redundant rotation costs more than it saves
+    // (LM head at 1 row 444 -> 482 us)
+    la.fuse_rot = (rows <= kFuseRotRows && stg.x_whole && weights < kFuseRotWeights) ? 1 : 0;
+    la.x = x;
     for (int i = 0; i < count; i++) {
       rc = encode_trellis_map(ws[i], f.ncol * 8 * bits, stg.H, &la.tm[i]);
       if (rc) return rc;
@@ -670,9 +684,11 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     ctas = ctas < S ? ctas : S;  // persistent: one CTA per SM at most
   }
   // everything that can fail on the host is done: enqueue the rotation, then the linear kernel
-  rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
-              pdl);
-  if (rc) return rc;
+  if (!la.fuse_rot) {
+    rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
+                pdl);
+    if (rc) return rc;
+  }
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && record_event(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");

@@ -58,6 +58,7 @@ struct Member {
   const uint32_t* trellis;  // first tile of this weight (or view)
   long long stride;         // uint32 words between tile rows
   const __half* svh;        // N
+  const __half* suh;        // K (read by the decode-rows kernel when it rotates x itself)
   const uint2* xf;          // rotated x in B-fragment order (see xf_index)
   void* y;                  // rows x N, act dtype
   float* partial;           // [pass][P][rp][N] FP32 subtree sums
@@ -85,6 +86,8 @@ struct LinearArgs {
   int ring_boxes;   // warp-granular kernel: trellis copies in flight per warp (R, 1 or 2)
   int x_rows;       // warp-granular kernel: tile rows per x stage (the whole chunk, or H)
   int x_whole;      // warp-granular kernel: 1 if one x stage holds the whole chunk
+  int fuse_rot;     // warp-granular kernel: 1 if each CTA rotates its chunk of x itself (few rows)
+  const void* x;    // the call's x (rows x K, act dtype), read when fuse_rot
   CUtensorMap tm[3];  // warp-granular kernel: member m's trellis as a 2-D tensor of uint32
                       // words (columns of the view x K/16 tile rows), box (NCOL*8*BITS, H)
 };
@@ -863,8 +866,44 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
       bulk_g2s(base + st * XS + q * XH * 256, M.xf + xf_index(q, t0 + (xw ? 0 : b * H), 0, a.TK),
                (uint32_t)(rows_b * 256), &xfull[st]);
   };
-  if (threadIdx.x == 0)
+  const bool fuse = a.fuse_rot != 0;  // only with a whole-chunk x stage (host-checked)
+  if (fuse) {
+    // rotate the chunk's x here instead of copying what the rotation kernel
+    // wrote: the 128-blocks overlapping the chunk, the call's real rows, the
+    // same arithmetic as the rotation kernel (rot_load, rot_member) and the
+    // same fragment order, into the zeroed x stage
+    RotArgs ra = {};
+    ra.x = a.x;
+    ra.suh[0] = M.suh;
+    ra.rows = a.rows;
+    ra.K = a.K;
+    ra.act = a.act;
+    uint4* z = reinterpret_cast<uint4*>(base);
+    for (int i = threadIdx.x; i < XS / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    const int b0 = (t0 * 16) >> 7, b1 = ((t0 + n) * 16 - 1) >> 7;
+    const int items = (b1 - b0 + 1) * a.rows;
+    uint32_t* xs32 = reinterpret_cast<uint32_t*>(base);
+    for (int it = warp; it < items; it += W) {
+      const int r = it / (b1 - b0 + 1), b = b0 + it % (b1 - b0 + 1);
+      float xv[4];
+      __half2 h[2];
+      rot_load(ra, r, b, lane, xv);
+      rot_member(ra, 0, b, lane, xv, h);
+      const int q = r >> 3, gq = r & 7;
+      const int tk = 8 * b + (lane >> 2);
+      const int reg = (lane & 3) >= 2 ? 1 : 0;
+      if (tk >= t0 && tk < t0 + n)
+#pragma unroll
+        for (int mm = 0; mm < 2; mm++) {
+          const int fl = 4 * gq + 2 * (lane & 1) + mm;
+          xs32[((q * XH + (tk - t0)) * 32 + fl) * 2 + reg] = *reinterpret_cast<const uint32_t*>(&h[mm]);
+        }
+    }
+    __syncthreads();
+  } else if (threadIdx.x == 0) {
     for (int b = 0; b < (xw ? 1 : R) && b < nbox; b++) load_x(b);
+  }
   float acc[NCOL][NR][4];
 #pragma unroll
   for (int c = 0; c < NCOL; c++)
@@ -877,7 +916,7 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
     const int st = b & (R - 1);
     const uint32_t par = (uint32_t)(b / R) & 1u;
     bool ok = mbar_wait_bounded(&wfull[warp][st], par);
-    if (xw ? b == 0 : true) ok = ok && mbar_wait_bounded(&xfull[xw ? 0 : st], xw ? 0u : par);
+    if (!fuse && (xw ? b == 0 : true)) ok = ok && mbar_wait_bounded(&xfull[xw ? 0 : st], xw ? 0u : par);
     if (!__all_sync(0xffffffffu, ok)) {
       alive = false;
       break;
