@@ -79,9 +79,11 @@ def test_group_equals_single_and_oracle(qkv, rows):
         assert_close(to_f64(yg), oracle_y(hw, x64), what=f"group N={hw.N} rows={rows}")
 
 
-def test_group_planted_controls_go_red(qkv):
-    # one member's suh swapped (rot_group) and one member's svh swapped must change bytes
-    x64, x = x_of(3, 7, 5120)
+@pytest.mark.parametrize("rows", [2, 7])
+def test_group_planted_controls_go_red(qkv, rows):
+    # one member's suh swapped (rot_group, or the in-kernel rotation at 2 rows)
+    # and one member's svh swapped must change bytes
+    x64, x = x_of(3, rows, 5120)
     (hq, q), (hk, k), (hv, v) = qkv
     ref = tfx.group([q, k, v], x)
     k_bad = tfx.Weight(k._keep[0], q._keep[1], k._keep[2], 5120, 1024, 4)
@@ -163,7 +165,7 @@ def test_variants_and_row_counts_byte_identical(K, N, act):
     tfx.set_variant(tfx.VARIANT_AUTO)
     ref = tfx.linear(w, x)  # 128 rows: mid kernel, NR = 16
     try:
-        for rows in (1, 7, 16, 17, 24, 32, 33, 48, 49, 64, 100, 128):
+        for rows in (1, 3, 4, 5, 7, 16, 17, 24, 32, 33, 48, 49, 64, 100, 128):
             for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP):
                 tfx.set_variant(var)
                 y = tfx.linear(w, x[:rows])
