@@ -44,6 +44,7 @@ constexpr int kTcMmaWarp = 20;
 constexpr int kTcXWarp = 21;
 constexpr int kTcThreads = 22 * 32;
 constexpr int kTcXS = 3;                              // x ring stages
+constexpr int kTcXLanes = 4;                          // lanes that copy a stage's x (one slice each)
 constexpr int kTcXStage = kTcSK * kTcRowsMax * 32;    // x bytes per stage (32 KB)
 constexpr int kTcAB = 3;                              // A (decoded weight) buffers
 constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (32 KB)
@@ -325,62 +326,76 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     lw.init(lane);
     const int g = lane >> 2, t = lane & 3;
     const int off0 = 512 * j + 16 * g + 4 * t;  // A-fragment register 0 in the core-matrix layout
-    // words of the next stage, loaded one stage ahead
-    uint32_t own[kH][WF::kOwn];
-    auto load_stage = [&](const TcUnit& U, int s0) {
+    // the words of stage gs sit in register slot gs % NS; the slot of the
+    // stage just decoded is refilled with the words NS-1 stages ahead, so a
+    // load has NS-1 stages of decode to land (the loop is unrolled NS times
+    // so that every slot is a fixed set of registers: no in-flight load is
+    // ever copied)
+    constexpr int NS = WF::kOwn <= 2 ? 3 : 2;
+    uint32_t own[NS][kH][WF::kOwn];
+    auto load_stage = [&](const TcUnit& U, int s0, uint32_t (&dst)[kH][WF::kOwn]) {
       const Member& M = a.m[U.mi];
       const uint32_t* col = M.trellis + (long long)(U.nb * 8 + j) * (8 * BITS);
 #pragma unroll
       for (int h = 0; h < kH; h++)
-        if (s0 + q0 + h < U.nsteps) WF::load(col + (long long)(U.tbeg + s0 + q0 + h) * M.stride, lw, lane, own[h]);
+        if (s0 + q0 + h < U.nsteps) WF::load(col + (long long)(U.tbeg + s0 + q0 + h) * M.stride, lw, lane, dst[h]);
     };
+    // stage iterators: (u, s0, U) the stage to decode, (lu, ls0, LU) the next one to load
     int u = blockIdx.x, s0 = 0, gs = 0;
     TcUnit U;
-    if (u < ta.units) {
-      U = tc_unit(ta, u);
-      load_stage(U, 0);
+    if (u < ta.units) U = tc_unit(ta, u);
+    int lu = u, ls0 = 0;
+    TcUnit LU = U;
+    auto advance = [&](int& uu, int& ss, TcUnit& UU) {
+      ss += kTcSK;
+      if (ss >= UU.nsteps) {
+        uu += gridDim.x;
+        ss = 0;
+        if (uu < ta.units) UU = tc_unit(ta, uu);
+      }
+    };
+#pragma unroll
+    for (int sl = 0; sl < NS - 1; sl++) {
+      if (lu < ta.units) {
+        load_stage(LU, ls0, own[sl]);
+        advance(lu, ls0, LU);
+      }
     }
     while (u < ta.units) {
-      const int cnt = min(kTcSK, U.nsteps - s0);
-      uint32_t cur[kH][WF::kOwn];
 #pragma unroll
-      for (int h = 0; h < kH; h++)
-#pragma unroll
-        for (int i = 0; i < WF::kOwn; i++) cur[h][i] = own[h][i];
-      // advance and prefetch the next stage's words (possibly of the next unit)
-      int u1 = u, s1 = s0 + kTcSK;
-      TcUnit U1 = U;
-      if (s1 >= U.nsteps) {
-        u1 = u + gridDim.x;
-        s1 = 0;
-        if (u1 < ta.units) U1 = tc_unit(ta, u1);
-      }
-      if (u1 < ta.units) load_stage(U1, s1);
-      const int ab = gs % kTcAB;
-      if (gs >= kTcAB) bar_sync(kBarFree + ab, kReadyThreads);
-      if (!s_abort) {
-        unsigned char* abuf = sA + ab * kTcAStage;
-#pragma unroll
-        for (int h = 0; h < kH; h++) {
-          if (q0 + h < cnt) {
-            uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
-            WF::gather(cur[h], lw, lane, raw);
-            lw.align(raw, win);
-            decode8<BITS>(win, af);
-            unsigned char* o = abuf + (q0 + h) * 4096 + off0;
-            *reinterpret_cast<uint32_t*>(o) = af[0];        // n = g,   k = 2t..
-            *reinterpret_cast<uint32_t*>(o + 256) = af[1];  // n = g+8, k = 2t..
-            *reinterpret_cast<uint32_t*>(o + 128) = af[2];  // n = g,   k = 2t+8..
-            *reinterpret_cast<uint32_t*>(o + 384) = af[3];  // n = g+8, k = 2t+8..
+      for (int sl = 0; sl < NS; sl++) {
+        if (u < ta.units) {
+          // refill the slot decoded last (stage gs-1) with stage gs+NS-1
+          if (lu < ta.units) {
+            load_stage(LU, ls0, own[(sl + NS - 1) % NS]);
+            advance(lu, ls0, LU);
           }
+          const int cnt = min(kTcSK, U.nsteps - s0);
+          const int ab = gs % kTcAB;
+          if (gs >= kTcAB) bar_sync(kBarFree + ab, kReadyThreads);
+          if (!s_abort) {
+            unsigned char* abuf = sA + ab * kTcAStage;
+#pragma unroll
+            for (int h = 0; h < kH; h++) {
+              if (q0 + h < cnt) {
+                uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
+                WF::gather(own[sl][h], lw, lane, raw);
+                lw.align(raw, win);
+                decode8<BITS>(win, af);
+                unsigned char* o = abuf + (q0 + h) * 4096 + off0;
+                *reinterpret_cast<uint32_t*>(o) = af[0];        // n = g,   k = 2t..
+                *reinterpret_cast<uint32_t*>(o + 256) = af[1];  // n = g+8, k = 2t..
+                *reinterpret_cast<uint32_t*>(o + 128) = af[2];  // n = g,   k = 2t+8..
+                *reinterpret_cast<uint32_t*>(o + 384) = af[3];  // n = g+8, k = 2t+8..
+              }
+            }
+            fence_async_smem();
+          }
+          bar_arrive(kBarReady + ab, kReadyThreads);
+          gs++;
+          advance(u, s0, U);
         }
-        fence_async_smem();
       }
-      bar_arrive(kBarReady + ab, kReadyThreads);
-      gs++;
-      u = u1;
-      s0 = s1;
-      U = U1;
     }
   } else if (warp < kTcFoldWarp0 + 4) {
     // ---------------- fold and output: thread = TMEM lane = column n of the block
@@ -456,36 +471,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         if (lane == 0) okx = mbar_wait(&xfull[xs], (gs / kTcXS) & 1, &s_abort, ta.err);
         okx = __shfl_sync(0xffffffffu, okx, 0);
         tc_fence_after();
-        uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
-        uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
+        const bool go = okx && !s_abort;
+        const uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
+        const uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
         const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
-        if (cnt == kTcSK && acc && s0 + kTcSK <= cnext) {
-          // the whole stage continues the current chunk: issue it back to back
-          if (lane == 0 && okx && !s_abort) {
-#pragma unroll
-            for (int q = 0; q < kTcSK; q++)
-              umma_f16(tmem + dcol, da + (uint64_t)(q * (4096 >> 4)), db + (uint64_t)(q * db_step), idesc, 1u);
-            if (s0 + kTcSK == cnext) umma_commit(&chunk_done[gc & 1]);
+        // the stage's k-steps as runs inside one chunk: a chunk start first
+        // resets the accumulator (and waits until its TMEM region was folded),
+        // then lane 0 issues the run back to back and, if the run ends the
+        // chunk, commits it to the fold warps
+        for (int q = 0; q < cnt;) {
+          if (s0 + q == cnext) {
+            ci++;
+            gc++;
+            acc = 0;
+            dcol = (uint32_t)((gc & 1) * NMf);
+            cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
+            // the region of chunk gc last held chunk gc-2: it must have been folded
+            if (gc >= 2) bar_sync(kBarFolded + (gc & 1), kFoldedThreads);
+            tc_fence_after();
           }
-        } else {
-          for (int q = 0; q < cnt; q++) {
-            const int i = s0 + q;
-            if (i == cnext) {
-              ci++;
-              gc++;
-              acc = 0;
-              dcol = (uint32_t)((gc & 1) * NMf);
-              cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
-              // the region of chunk gc last held chunk gc-2: it must have been folded
-              if (gc >= 2) bar_sync(kBarFolded + (gc & 1), kFoldedThreads);
-              tc_fence_after();
-            }
-            if (lane == 0 && okx && !s_abort) umma_f16(tmem + dcol, da, db, idesc, acc);
-            acc = 1;
-            if (lane == 0 && i + 1 == cnext) umma_commit(&chunk_done[gc & 1]);
-            da += 4096 >> 4;
-            db += db_step;
+          const int qe = min(cnt, cnext - s0);
+          if (lane == 0) {
+            if (go)
+              for (int i = q; i < qe; i++) {
+                umma_f16(tmem + dcol, da + (uint64_t)(i * (4096 >> 4)), db + (uint64_t)(i * db_step), idesc, acc);
+                acc = 1;
+              }
+            if (s0 + qe == cnext) umma_commit(&chunk_done[gc & 1]);
           }
+          acc = 1;
+          q = qe;
         }
         if (lane == 0) {
           umma_commit(&sdone[ab]);  // frees A buffer ab and x slot xs (the same index)
@@ -508,8 +523,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     for (int c = gc - 1; c <= gc; c++)
       if (c >= 0) bar_sync(kBarFolded + (c & 1), kFoldedThreads);
   } else {
-    // ---------------- x rows of the pass: one contiguous run per stage
-    if (lane == 0) {
+    // ---------------- x rows of the pass: one contiguous run per stage, cut
+    // into kTcXLanes slices that as many lanes copy: the bulk copies of one
+    // thread complete one after another (measured on GB300: about one per
+    // 0.45 us whatever their size up to 64 KB), those of different threads overlap
+    if (lane < kTcXLanes) {
+      constexpr unsigned kMask = (1u << kTcXLanes) - 1;
       int gs = 0;
       for (int u = blockIdx.x; u < ta.units; u += gridDim.x) {
         const TcUnit U = tc_unit(ta, u);
@@ -519,11 +538,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
           const int cnt = min(kTcSK, U.nsteps - s0);
           const int xs = gs % kTcXS;
-          if (gs >= kTcXS && !mbar_wait(&sdone[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, 32)) continue;
-          if (s_abort) continue;
-          const uint32_t bytes = (uint32_t)(cnt * U.NMp * 32);
-          mbar_expect_tx(&xfull[xs], bytes);
-          bulk_g2s(sX + xs * kTcXStage, xsrc + (long long)(U.tbeg + s0) * U.NMp * 32, bytes, &xfull[xs]);
+          int ok = 1;
+          if (lane == 0 && gs >= kTcXS) ok = mbar_wait(&sdone[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, 32);
+          ok = __shfl_sync(kMask, ok, 0);
+          if (!ok || s_abort) continue;
+          // bytes = cnt * NMp * 32 is a multiple of 512: every slice is a multiple of 16 bytes
+          const uint32_t bytes = (uint32_t)(cnt * U.NMp * 32), slice = bytes / kTcXLanes;
+          if (lane == 0) mbar_expect_tx(&xfull[xs], bytes);
+          __syncwarp(kMask);
+          bulk_g2s(sX + xs * kTcXStage + lane * slice,
+                   xsrc + (long long)(U.tbeg + s0) * U.NMp * 32 + (long long)lane * slice, slice, &xfull[xs]);
         }
       }
       if (s_abort) {
