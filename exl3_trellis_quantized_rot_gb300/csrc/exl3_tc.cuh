@@ -24,10 +24,13 @@
 //                 FP32 slab, which tc_combine_kernel folds afterwards;
 //   warp 20       issues the MMAs strictly in k order (lane 0);
 //   warp 21       bulk-copies the x rows of each stage (lane 0).
-// Hand-offs between the decode warps, the MMA warp and the fold warps use
-// hardware named barriers (waiting warps are descheduled, nothing polls);
-// completions of the asynchronous units (bulk copies, MMAs) are mbarriers that
-// one lane polls. Every mbarrier wait is bounded: on a timeout the kernel
+// The decode warps hand a filled A buffer to the MMA warp, and the fold warps
+// hand a folded TMEM region back to it, through hardware named barriers
+// (waiting warps are descheduled, nothing polls); completions of the
+// asynchronous units (bulk copies, MMAs) are mbarriers that lane 0 of each
+// waiting warp polls: the decode warps and the x warp wait on the MMA
+// completion of the buffer they refill themselves, so that the MMA warp's
+// loop is only ready barrier, x wait, MMA issue and commit. Every mbarrier wait is bounded: on a timeout the kernel
 // records an error and from then on skips all work while still taking every
 // named barrier, so each warp reaches the end and TMEM is released.
 #pragma once
@@ -54,8 +57,7 @@ constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kT
 // named barriers (0 is __syncthreads)
 constexpr int kBarFold = 1;        // the 4 fold warps
 constexpr int kBarReady = 2;       // + A buffer: decode warps -> MMA warp (3 ids)
-constexpr int kBarFree = 5;        // + A buffer: MMA warp -> decode warps (3 ids)
-constexpr int kBarFolded = 8;      // + chunk parity: fold warps -> MMA warp (2 ids)
+constexpr int kBarFolded = 5;      // + chunk parity: fold warps -> MMA warp (2 ids)
 constexpr int kReadyThreads = (kTcDecodeWarps + 1) * 32;
 constexpr int kFoldedThreads = 5 * 32;
 
@@ -259,13 +261,6 @@ __device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane,
   }
 }
 
-// Stages of this CTA's units (the same count in every role).
-__device__ __forceinline__ int tc_stages_of_cta(const TcArgs& ta) {
-  int n = 0;
-  for (int u = blockIdx.x; u < ta.units; u += gridDim.x) n += (tc_unit(ta, u).nsteps + kTcSK - 1) / kTcSK;
-  return n;
-}
-
 template <int BITS>
 __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_constant__ TcArgs ta) {
   using WF = WordFetch<BITS>;
@@ -372,7 +367,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           }
           const int cnt = min(kTcSK, U.nsteps - s0);
           const int ab = gs % kTcAB;
-          if (gs >= kTcAB) bar_sync(kBarFree + ab, kReadyThreads);
+          // buffer ab last held stage gs - kTcAB: wait until its MMAs completed
+          if (gs >= kTcAB) {
+            if (lane == 0) mbar_wait(&sdone[ab], ((gs - kTcAB) / kTcAB) & 1, &s_abort, ta.err);
+            __syncwarp();
+          }
           if (!s_abort) {
             unsigned char* abuf = sA + ab * kTcAStage;
 #pragma unroll
@@ -452,7 +451,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     }
   } else if (warp == kTcMmaWarp) {
     // ---------------- MMA issue, strictly in k order; lane 0 issues, the warp takes the barriers
-    const int total = tc_stages_of_cta(ta);
     const uint64_t da0 = umma_desc(sA), db0 = umma_desc(sX);
     int gs = 0, gc = -1;
     for (int u = blockIdx.x; u < ta.units; u += gridDim.x) {
@@ -502,24 +500,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           acc = 1;
           q = qe;
         }
-        if (lane == 0) {
-          umma_commit(&sdone[ab]);  // frees A buffer ab and x slot xs (the same index)
-        }
+        // frees A buffer ab and x slot xs (the same index): the decode warps
+        // and the x warp wait on it themselves
+        if (lane == 0) umma_commit(&sdone[ab]);
         __syncwarp();
-        // release the A buffer of the previous stage once its MMAs are done
-        const int r = gs - 1;
-        if (r >= 0 && r + kTcAB < total) {
-          if (lane == 0) mbar_wait(&sdone[r % kTcAB], (r / kTcAB) & 1, &s_abort, ta.err);
-          __syncwarp();
-          bar_arrive(kBarFree + r % kTcAB, kReadyThreads);
-        }
       }
     }
-    // the last stage's buffer, then the folds of the last two chunks
-    {
-      const int r = gs - 1;
-      if (r >= 0 && r + kTcAB < total) bar_arrive(kBarFree + r % kTcAB, kReadyThreads);
-    }
+    // the folds of the last two chunks
     for (int c = gc - 1; c <= gc; c++)
       if (c >= 0) bar_sync(kBarFolded + (c & 1), kFoldedThreads);
   } else {
