@@ -765,12 +765,18 @@ __device__ __forceinline__ void cluster_fold(const float* local, float (&v)[4]) 
 
 // Rotate one row of a 128-column block back and store it: FWHT over the 128
 // values (4 per lane), x 1/sqrt(128), x svh, round to the output dtype.
-__device__ __forceinline__ void rot_out_row(float (&v)[4], const __half* svh, void* y, long long yo, int act,
-                                            int lane) {
+// sv4 holds the lane's 4 svh values (read before the caller's barriers, so
+// that no global load sits on the epilogue's critical path).
+__device__ __forceinline__ void rot_out_row(float (&v)[4], uint2 sv4, void* y, long long yo, int act, int lane) {
   fwht128(v, lane);
   float sv[4];
-#pragma unroll
-  for (int e = 0; e < 4; e++) sv[e] = __half2float(svh[e]);
+  {
+    const __half2 s01 = *reinterpret_cast<const __half2*>(&sv4.x), s23 = *reinterpret_cast<const __half2*>(&sv4.y);
+    sv[0] = __low2float(s01);
+    sv[1] = __high2float(s01);
+    sv[2] = __low2float(s23);
+    sv[3] = __high2float(s23);
+  }
 #pragma unroll
   for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
   uint2 out;
@@ -911,6 +917,14 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
     for (int q = 0; q < NR; q++) acc[c][q][0] = acc[c][q][1] = acc[c][q][2] = acc[c][q][3] = 0.f;
   LaneWindow<BITS> lw;
   lw.init(lane);
+  // svh of this lane's 4 output columns for the warps that fold a row at the
+  // end (svh is 16-byte aligned and a view starts on a 128-column block). With
+  // one row group (rows <= 8) it is read now, so that no global load sits on
+  // the epilogue's critical path: at one row the CTA of chunk 0 folds the
+  // whole row after the others wait for it (measured 0.5 us per call)
+  uint2 sv4 = make_uint2(0u, 0u);
+  if constexpr (NR == 1)
+    if (chunk + warp * M.C < a.rows) sv4 = *reinterpret_cast<const uint2*>(M.svh + nb * 128 + 4 * lane);
   bool alive = true;
   for (int b = 0; b < nbox && alive; b++) {
     const int st = b & (R - 1);
@@ -1000,6 +1014,10 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
       }
   }
   cluster_sync();
+  // with more than one row group, svh is read here, where its latency overlaps
+  // the distributed shared-memory loads of the fold
+  if constexpr (NR > 1)
+    if (chunk + warp * M.C < a.rows) sv4 = *reinterpret_cast<const uint2*>(M.svh + nb * 128 + 4 * lane);
   // rows chunk, chunk + C, ... of this block: one warp per row
   for (int r = chunk + warp * M.C; r < a.rows && !dead; r += W * M.C) {
     float v[4];
@@ -1011,7 +1029,7 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
       case 8: cluster_fold<8>(src, v); break;
       default: cluster_fold<16>(src, v); break;
     }
-    rot_out_row(v, M.svh + nb * 128 + 4 * lane, M.y, (long long)r * M.N + nb * 128 + 4 * lane, a.act, lane);
+    rot_out_row(v, sv4, M.y, (long long)r * M.N + nb * 128 + 4 * lane, a.act, lane);
   }
   cluster_sync();
 }
