@@ -137,6 +137,15 @@ def barrier(ws: int):
         dist.barrier()
 
 
+def whole_job(ms_local: float, steps: int, ws: int, device) -> tuple[float, float]:
+    """Whole-job throughput of N replicas: every rank streams STEP_WEIGHT_BYTES
+    per step, and the slowest rank's time over the timed steps decides.
+    Returns (max ms over ranks, GB/s of all ranks together)."""
+    ms_max = reduce_max(ms_local, ws, device)
+    sec_per_step = ms_max / 1e3 / steps
+    return ms_max, ws * STEP_WEIGHT_BYTES / sec_per_step / 1e9
+
+
 # ---------------------------------------------------------------------------- CPU oracle leg
 
 def oracle_sample(seconds_budget: float = 15.0):
@@ -288,9 +297,8 @@ def run_gpu(args):
         barrier(ws)
     clocks = clk.summary()
     ms = start.elapsed_time(stop)
-    ms_max = reduce_max(ms, ws, dev)
+    ms_max, value = whole_job(ms, args.steps, ws, dev)
     sec_per_step = ms_max / 1e3 / args.steps
-    value = ws * STEP_WEIGHT_BYTES / sec_per_step / 1e9
     del g_steps
 
     # dominant kernel: the linear kernel of each call (group launch and single
