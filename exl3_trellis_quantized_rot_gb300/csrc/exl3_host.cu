@@ -259,15 +259,14 @@ int row_tile(int rows) { return rows <= 8 ? 0 : rows <= 16 ? 1 : rows <= 32 ? 2 
 constexpr int kFuseRotRows = 4;
 constexpr long long kFuseRotWeights = 64LL << 20;
 
-// Kernel choice. auto: up to 64 rows the warp-granular decode-rows kernel,
-// except 33..64 rows on calls of at least kTcMidWeights weights, which go to
-// the persistent tensor-core kernel like every call above 64 rows (measured on
-// GB300: 5120 x 2*17408 at 64 rows 155 us against 180 us for the decode-rows
-// kernel). The other variants force a family where it serves the row count
-// (all give the same bytes).
-constexpr long long kTcMidWeights = 64LL << 20;
-
-Family pick(int bits, int rows, long long weights = 0) {
+// Kernel choice. auto: up to 32 rows the warp-granular decode-rows kernel,
+// above that the persistent tensor-core kernel (measured on GB300, 4-bit,
+// K = 5120, graph-replayed calls: at 40..64 rows 5120 x 5120 34-35 us against
+// 43-47 us, the q/k/v group 39-40 us against 69-75 us, gate+up 128-131 us
+// against 251-275 us; at 24..32 rows the decode-rows kernel is faster or even).
+// The other variants force a family where it serves the row count (all give
+// the same bytes).
+Family pick(int bits, int rows) {
   const tfx::KernelSet& ks = kernels(bits);
   const int i = rows <= tfx::kRowsMaxRows ? row_tile(rows) : 0;
   const int ncol = i < 2 ? 2 : 1;  // must match the instantiations in exl3_bits.cu
@@ -279,7 +278,7 @@ Family pick(int bits, int rows, long long weights = 0) {
     case 2: return tc;
     case 3: return rows <= tfx::kRowsMaxRows ? warpk : tc;
     default:
-      if (rows <= 32 || (rows <= tfx::kRowsMaxRows && weights < kTcMidWeights)) return warpk;
+      if (rows <= 32) return warpk;
       return tc;
   }
 }
@@ -568,7 +567,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ra.rows_pad = (rows + 15) / 16 * 16;
   long long weights = 0;
   for (int i = 0; i < count; i++) weights += (long long)K * ws[i]->N;
-  const Family f = pick(bits, rows, weights);
+  const Family f = pick(bits, rows);
   if (f.rows()) ra.rows_pad = tfx::x_rows_padded(rows);  // whole row tiles, zero-padded
   ra.K = K;
   ra.act = ws[0]->act;

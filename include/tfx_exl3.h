@@ -131,11 +131,10 @@ int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk);
 /* Allocations and counter memsets made for this weight since its creation. */
 int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
 
-/* Kernel family for the next calls. 0 = auto: 1..64 rows the warp-granular
+/* Kernel family for the next calls. 0 = auto: 1..32 rows the warp-granular
  * decode-rows kernel (one cluster of C CTAs per 128-column block folds the C
- * chunk sums in distributed shared memory), except 33..64 rows on calls of at
- * least 64 Mi weights, which go to the tensor-core kernel like every call
- * above 64 rows; 1 = for 1..64 rows the CTA decode-rows kernel whose split-K
+ * chunk sums in distributed shared memory), every call above 32 rows the
+ * tensor-core kernel; 1 = for 1..64 rows the CTA decode-rows kernel whose split-K
  * partials are summed in-kernel by the last CTA to arrive on each block's
  * counter (the counter resets itself); 2 = the tensor-core kernel for every
  * row count; 3 = the warp-granular decode-rows kernel for every call of
