@@ -17,22 +17,26 @@
 // (member, pass, 128-column block, chunk group) in a fixed stride. The work
 // of a unit is cut into stages of kTcSK k-steps that flow through warp roles:
 //   warps 0..15   decode: load their tiles' words straight from global memory
-//                 one stage ahead and turn 4 tiles per stage into FP16 A operands;
+//                 into a ring of register slots (up to two stages ahead) and
+//                 turn 4 tiles per stage into FP16 A operands;
 //   warps 16..19  fold: merge each finished chunk into the chunk tree (levels
 //                 parked in TMEM), then write the unit's output: the whole
 //                 rot_out epilogue when one unit covers all C chunks, else its
 //                 FP32 slab, which tc_combine_kernel folds afterwards;
 //   warp 20       issues the MMAs strictly in k order (lane 0);
-//   warp 21       bulk-copies the x rows of each stage (lane 0).
+//   warp 21       bulk-copies the x rows of each stage (lanes 0..3, a slice each).
 // The decode warps hand a filled A buffer to the MMA warp, and the fold warps
 // hand a folded TMEM region back to it, through hardware named barriers
-// (waiting warps are descheduled, nothing polls); completions of the
+// (waiting warps are descheduled, nothing polls). Completions of the
 // asynchronous units (bulk copies, MMAs) are mbarriers that lane 0 of each
-// waiting warp polls: the decode warps and the x warp wait on the MMA
+// waiting warp polls; the decode warps and the x warp wait on the MMA
 // completion of the buffer they refill themselves, so that the MMA warp's
-// loop is only ready barrier, x wait, MMA issue and commit. Every mbarrier wait is bounded: on a timeout the kernel
-// records an error and from then on skips all work while still taking every
-// named barrier, so each warp reaches the end and TMEM is released.
+// loop is only ready barrier, x wait, MMA issue and commit. A waiter cannot
+// fall two phases behind on such a barrier: its next completion needs the
+// waiter's own next stage first. Every mbarrier wait is bounded: on a
+// timeout the kernel records an error and from then on skips all work while
+// still taking every named barrier, so each warp reaches the end and TMEM is
+// released.
 #pragma once
 #include "exl3_kernels.cuh"
 
