@@ -287,9 +287,12 @@ Family pick(int bits, int rows) {
 // rows run as one pass; longer calls use 64-row passes so that every unit can
 // hold all C chunks (P = 1, no slabs). Otherwise G is the power of two that
 // minimises the persistent CTAs' critical path, ceil(units / SMs) unit
-// lengths plus a fixed per-unit cost, among those whose TMEM regions fit:
-// (2 + log2 G) * rows columns <= 512. Launch shape only: the bits do not
-// depend on G.
+// lengths plus a fixed per-unit cost of 16 k-steps (pipeline fill and fold;
+// measured on GB300 by forcing each G: 5120 x 5120 at 40/64/128 rows best at
+// G = 2, 32.3/33.0/36.0 us against 33.8/34.8/39.6 us at G = 1, which a cost of
+// 8 k-steps chose; the q/k/v group and gate+up keep their G), among those whose
+// TMEM regions fit: (2 + log2 G) * rows columns <= 512. Launch shape only: the
+// bits do not depend on G.
 int tc_rows_per_pass(int rows) { return rows <= tfx::kTcRowsMax ? tfx::kTcRowsMax : tfx::kTcRowsLong; }
 int tc_passes(int rows) {
   const int rp = tc_rows_per_pass(rows);
@@ -305,7 +308,7 @@ int tc_group(long long blocks, int rows, int C, int TK) {
   for (int g = C; g >= 1; g /= 2) {
     if ((2 + __builtin_ctz(g)) * nm > 512) continue;
     const long long units = blocks * passes * (C / g);
-    const long long cost = (units + S - 1) / S * ((long long)TK * g / C + 8);
+    const long long cost = (units + S - 1) / S * ((long long)TK * g / C + 16);
     if (best_cost < 0 || cost < best_cost) {
       best = g;
       best_cost = cost;
