@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   griddep_wait();
   griddep_launch();
   {
-    // the launch must provide the shared memory this build lays out
+    // the launch must provide the shared memory the kernel lays out
     uint32_t dyn;
     asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
     if (dyn < kTcDynSmem) {
