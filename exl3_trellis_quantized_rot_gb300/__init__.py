@@ -25,7 +25,7 @@ ABI_SYMBOLS = ("tfx_exl3_linear", "tfx_exl3_group", "tfx_exl3_columns", "tfx_exl
                "tfx_exl3_release", "tfx_exl3_reset_counters", "tfx_exl3_debug_decode", "tfx_exl3_plan",
                "tfx_exl3_stats", "tfx_exl3_set_variant", "tfx_exl3_set_pdl", "tfx_exl3_debug_set_driver",
                "tfx_exl3_debug_mark_events", "tfx_exl3_linear_static", "tfx_exl3_debug_error",
-               "tfx_exl3_last_error")
+               "tfx_exl3_debug_launch_shape", "tfx_exl3_last_error")
 
 
 class WeightStruct(C.Structure):
@@ -77,6 +77,7 @@ def lib() -> C.CDLL:
         L.tfx_exl3_debug_mark_events.argtypes = [vp, vp]
         L.tfx_exl3_linear_static.argtypes = [W, vp, i, vp, vp]
         L.tfx_exl3_debug_error.argtypes = [W, C.POINTER(i)]
+        L.tfx_exl3_debug_launch_shape.argtypes = [i, i, i, C.c_int64, i, C.POINTER(i), C.POINTER(i)]
         L.tfx_exl3_last_error.restype = C.c_char_p
         for n in ABI_SYMBOLS[:-1]:
             getattr(L, n).restype = C.c_int
@@ -238,6 +239,16 @@ def device_error(w: Weight) -> int:
 
 def set_variant(v: int) -> int:
     return lib().tfx_exl3_set_variant(v)
+
+
+FAMILY_ROWS_CTA, FAMILY_ROWS_WARP, FAMILY_TENSOR = 0, 1, 2
+
+
+def debug_launch_shape(K: int, bits: int, rows: int, blocks: int, sm_count: int = 0):
+    """(family, chunks per tensor-core unit) that a call would launch; host only."""
+    f, g = C.c_int(), C.c_int()
+    _check(lib().tfx_exl3_debug_launch_shape(K, bits, rows, blocks, sm_count, C.byref(f), C.byref(g)))
+    return f.value, g.value
 
 
 def set_pdl(on: bool) -> int:

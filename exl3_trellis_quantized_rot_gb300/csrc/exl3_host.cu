@@ -298,11 +298,10 @@ int tc_passes(int rows) {
   const int rp = tc_rows_per_pass(rows);
   return (rows + rp - 1) / rp;
 }
-int tc_group(long long blocks, int rows, int C, int TK) {
+int tc_group(long long blocks, int rows, int C, int TK, long long S) {
   const int passes = tc_passes(rows);
   if (rows > tfx::kTcRowsMax) return C;
   const int nm = (rows + 15) / 16 * 16;
-  const long long S = sm_count();
   int best = 1;
   long long best_cost = -1;
   for (int g = C; g >= 1; g /= 2) {
@@ -599,7 +598,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   if (f.kind == kTensor) {
     long long blocks = 0;
     for (int i = 0; i < count; i++) blocks += ws[i]->N / 128;
-    tcG = tc_group(blocks, rows, chunks_of(K), K / 16);
+    tcG = tc_group(blocks, rows, chunks_of(K), K / 16, sm_count());
   }
   for (int i = 0; i < count; i++) {
     const tfx_exl3_weight* w = ws[i];
@@ -806,6 +805,19 @@ int tfx_exl3_debug_decode(const tfx_exl3_weight* w, uint16_t* W_out, cudaStream_
   da.N = w->N;
   const long long tiles = (long long)(w->K / 16) * (w->N / 16);
   return launch(kernels(w->bits).decode, dim3((unsigned)((tiles + 7) / 8)), dim3(256), 0, stream, &da, false);
+}
+
+int tfx_exl3_debug_launch_shape(int K, int bits, int rows, int64_t blocks, int sm_count_, int* family,
+                                int* chunks_per_unit) {
+  if (K <= 0 || K % 128 || bits < 1 || bits > 8 || rows < 1 || blocks < 1 || sm_count_ < 0 || !family ||
+      !chunks_per_unit)
+    return fail(TFX_EINVAL, "debug_launch_shape: K a positive multiple of 128, bits 1..8, rows >= 1, "
+                            "blocks >= 1, sm_count >= 0, non-null outputs");
+  const Family f = pick(bits, rows);
+  *family = (int)f.kind;
+  *chunks_per_unit =
+      f.kind == kTensor ? tc_group(blocks, rows, tfx::chunks_of(K), K / 16, sm_count_ ? sm_count_ : sm_count()) : 0;
+  return 0;
 }
 
 int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk) {

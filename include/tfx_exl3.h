@@ -143,6 +143,19 @@ int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
  * (auto|rows|mid|warp). Returns the previous value. */
 int tfx_exl3_set_variant(int variant);
 
+/* Introspection, host only (no GPU needed): the kernel family and tensor-core
+ * unit size that a call of `rows` rows over weights of this K and bits, with
+ * `blocks` 128-column blocks over all members, would launch under the current
+ * variant on a GPU of sm_count SMs (0 = the current device's, 152 when none is
+ * visible). *family: 0 = decode-rows CTA kernel (variant rows), 1 = warp-
+ * granular decode-rows kernel, 2 = tensor-core kernel. *chunks_per_unit: the
+ * chunks of K per tensor-core work unit (G; a launch-shape choice that never
+ * changes the bits), 0 for the decode-rows families. TFX_EINVAL on K not a
+ * positive multiple of 128, bits outside 1..8, rows or blocks < 1,
+ * sm_count < 0 or a null output. */
+int tfx_exl3_debug_launch_shape(int K, int bits, int rows, int64_t blocks, int sm_count, int* family,
+                                int* chunks_per_unit);
+
 /* Programmatic dependent launch on (1) or off (0); initial value from
  * TFX_EXL3_PDL=1 (default off). Returns the previous value. */
 int tfx_exl3_set_pdl(int on);

@@ -205,3 +205,53 @@ def test_variant_and_pdl_switches(L):
     assert tfx.set_variant(old) == tfx.VARIANT_MID
     old = tfx.set_pdl(False)
     assert tfx.set_pdl(old) == 0
+
+
+def test_kernel_choice_and_tensor_core_unit_size(L):
+    """The launch-shape rules (host only): auto sends 1..32 rows to the
+    warp-granular decode-rows kernel and every longer call to the tensor-core
+    kernel; the tensor-core unit size G (chunks of K per unit) is the measured
+    best for the 27B shapes on 152 SMs and always fits TMEM; forced variants
+    serve the row counts they cover. None of this changes the bits (the GPU
+    parity tests compare the families byte for byte)."""
+    shape = tfx.debug_launch_shape
+    old = tfx.set_variant(tfx.VARIANT_AUTO)
+    try:
+        for rows in (1, 7, 8, 9, 16, 17, 31, 32):
+            assert shape(5120, 4, rows, 40, 152) == (tfx.FAMILY_ROWS_WARP, 0), rows
+        for rows in (33, 48, 64, 65, 100, 128, 129, 4096):
+            assert shape(5120, 4, rows, 40, 152)[0] == tfx.FAMILY_TENSOR, rows
+        # G on 152 SMs, K = 5120 (16 chunks): 5120 x 5120 (40 blocks), the q/k/v group (64 blocks), gate+up (272)
+        want = {(40, 64): 2, (40, 128): 2, (64, 64): 8, (64, 128): 4, (272, 64): 16, (272, 128): 4}
+        for (blocks, rows), g in want.items():
+            assert shape(5120, 4, rows, blocks, 152) == (tfx.FAMILY_TENSOR, g), (blocks, rows)
+        # above 128 rows every unit holds all C chunks (64-row passes, no slabs)
+        assert shape(5120, 4, 4096, 136, 152) == (tfx.FAMILY_TENSOR, 16)
+        assert shape(1024, 4, 200, 8, 152) == (tfx.FAMILY_TENSOR, 16)
+        # G is a power of two dividing C whose TMEM regions fit: (2 + log2 G) * rows16 <= 512 columns
+        for K in (256, 1024, 5120, 17408):
+            c = min(16, K // 64)
+            c = 1 << (c.bit_length() - 1)
+            for rows in (33, 40, 64, 96, 128):
+                for blocks in (1, 8, 40, 64, 272, 1940):
+                    for sms in (1, 152, 1000):
+                        f, g = shape(K, 4, rows, blocks, sms)
+                        assert f == tfx.FAMILY_TENSOR
+                        assert g >= 1 and g & (g - 1) == 0 and c % g == 0, (K, rows, blocks, sms, g)
+                        assert (2 + g.bit_length() - 1) * ((rows + 15) // 16 * 16) <= 512
+        # forced families
+        tfx.set_variant(tfx.VARIANT_MID)
+        assert shape(5120, 4, 1, 40, 152)[0] == tfx.FAMILY_TENSOR
+        tfx.set_variant(tfx.VARIANT_WARP)
+        assert shape(5120, 4, 64, 40, 152) == (tfx.FAMILY_ROWS_WARP, 0)
+        assert shape(5120, 4, 65, 40, 152)[0] == tfx.FAMILY_TENSOR
+        tfx.set_variant(tfx.VARIANT_ROWS)
+        assert shape(5120, 4, 64, 40, 152) == (tfx.FAMILY_ROWS_CTA, 0)
+        assert shape(5120, 4, 65, 40, 152)[0] == tfx.FAMILY_TENSOR
+    finally:
+        tfx.set_variant(old)
+    for bad in ((100, 4, 1, 1, 152), (5120, 0, 1, 1, 152), (5120, 9, 1, 1, 152), (5120, 4, 0, 1, 152),
+                (5120, 4, 1, 0, 152), (5120, 4, 1, 1, -1)):
+        with pytest.raises(tfx.TfxError) as e:
+            shape(*bad)
+        assert e.value.code == tfx.EINVAL, bad
