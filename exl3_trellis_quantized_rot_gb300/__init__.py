@@ -25,7 +25,8 @@ ABI_SYMBOLS = ("tfx_exl3_linear", "tfx_exl3_group", "tfx_exl3_columns", "tfx_exl
                "tfx_exl3_release", "tfx_exl3_reset_counters", "tfx_exl3_debug_decode", "tfx_exl3_plan",
                "tfx_exl3_stats", "tfx_exl3_set_variant", "tfx_exl3_set_pdl", "tfx_exl3_debug_set_driver",
                "tfx_exl3_debug_mark_events", "tfx_exl3_linear_static", "tfx_exl3_debug_error",
-               "tfx_exl3_debug_launch_shape", "tfx_exl3_last_error")
+               "tfx_exl3_debug_launch_shape", "tfx_exl3_group_into", "tfx_exl3_debug_set_spin_limit",
+               "tfx_exl3_debug_decode_rate", "tfx_exl3_last_error")
 
 
 class WeightStruct(C.Structure):
@@ -78,9 +79,14 @@ def lib() -> C.CDLL:
         L.tfx_exl3_linear_static.argtypes = [W, vp, i, vp, vp]
         L.tfx_exl3_debug_error.argtypes = [W, C.POINTER(i)]
         L.tfx_exl3_debug_launch_shape.argtypes = [i, i, i, C.c_int64, i, C.POINTER(i), C.POINTER(i)]
+        L.tfx_exl3_group_into.argtypes = [C.POINTER(W), i, vp, i, C.POINTER(vp), C.POINTER(C.c_int64),
+                                          C.POINTER(i), vp]
+        L.tfx_exl3_debug_set_spin_limit.argtypes = [C.c_int64]
+        L.tfx_exl3_debug_decode_rate.argtypes = [i, i, vp, C.POINTER(i), C.POINTER(C.c_int64), vp]
         L.tfx_exl3_last_error.restype = C.c_char_p
         for n in ABI_SYMBOLS[:-1]:
             getattr(L, n).restype = C.c_int
+        L.tfx_exl3_debug_set_spin_limit.restype = C.c_int64
         _lib = L
     return _lib
 
@@ -201,6 +207,35 @@ def group(ws, x, rows: int | None = None, ys=None, stream=None):
     return ys
 
 
+def group_into(ws, x, ys, ldy, col0, rows: int | None = None, stream=None):
+    """tfx_exl3_group with an output window per member: member i's element
+    (r, n >= col0[i]) goes to ys[i] + r*ldy[i] + (n - col0[i]). ys are device
+    pointers or tensors (a tensor's data_ptr is the window's first element)."""
+    if rows is None:
+        rows = x.shape[0]
+    n = len(ws)
+    arr = (C.POINTER(WeightStruct) * max(n, 1))(*[C.pointer(w.s) for w in ws])
+    yarr = (C.c_void_p * max(n, 1))(*[_ptr(y) for y in ys])
+    larr = (C.c_int64 * max(n, 1))(*ldy)
+    carr = (C.c_int * max(n, 1))(*col0)
+    _check(lib().tfx_exl3_group_into(arr, n, _ptr(x), rows, yarr, larr, carr, _stream(stream)))
+
+
+def pack_spans(views, x, out, col0, rows: int | None = None, stream=None):
+    """Several column views of one weight packed side by side into `out`
+    (rows x sum of kept columns): view i keeps its columns from col0[i] on and
+    lands right after view i-1's kept columns, all in one call."""
+    ld = out.shape[1]
+    ys, off = [], 0
+    for v, c in zip(views, col0):
+        ys.append(out.data_ptr() + off * out.element_size())
+        off += v.N - c
+    if off != ld:
+        raise ValueError(f"kept columns {off} != out width {ld}")
+    group_into(views, x, ys, [ld] * len(views), list(col0), rows, stream)
+    return out
+
+
 def columns(w: Weight, start: int, n: int) -> Weight:
     """View of whole 128-column blocks [start, start+n) sharing w's memory."""
     v = Weight.__new__(Weight)
@@ -231,7 +266,9 @@ def stats(w: Weight):
 
 
 def device_error(w: Weight) -> int:
-    """1 if a tensor-core launch on w gave up a bounded wait, else 0."""
+    """The weight's device error word: 1 a tensor-core launch gave up a bounded
+    wait, 2 a tensor-core launch had too little shared memory, 3 a decode-rows
+    launch gave up waiting for a copy; 0 otherwise."""
     e = C.c_int()
     _check(lib().tfx_exl3_debug_error(w.ref(), C.byref(e)))
     return e.value
@@ -249,6 +286,21 @@ def debug_launch_shape(K: int, bits: int, rows: int, blocks: int, sm_count: int 
     f, g = C.c_int(), C.c_int()
     _check(lib().tfx_exl3_debug_launch_shape(K, bits, rows, blocks, sm_count, C.byref(f), C.byref(g)))
     return f.value, g.value
+
+
+def set_spin_limit(clocks: int) -> int:
+    """Clock cycles a bounded wait in a kernel polls before it gives up (<= 0:
+    the default, about 1 s). Returns the previous limit. For tests."""
+    return lib().tfx_exl3_debug_set_spin_limit(clocks)
+
+
+def decode_rate(bits: int, tiles_per_warp: int, sink=None, stream=None):
+    """Launch the decode-rate probe (no global traffic); returns (weights decoded,
+    floats the sink needs). With sink None nothing is launched."""
+    nf, nw = C.c_int(), C.c_int64()
+    _check(lib().tfx_exl3_debug_decode_rate(bits, tiles_per_warp, _ptr(sink) if sink is not None else None,
+                                            C.byref(nf), C.byref(nw), _stream(stream) if sink is not None else None))
+    return nw.value, nf.value
 
 
 def set_pdl(on: bool) -> int:

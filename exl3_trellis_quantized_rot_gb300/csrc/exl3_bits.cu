@@ -56,6 +56,7 @@ KernelSet TFX_CAT(kernels_b, TFX_BITS)() {
   k.linear_warp[3] = reinterpret_cast<const void*>(&linear_warp_kernel<TFX_BITS, 8, 1>);
   k.linear_tc = reinterpret_cast<const void*>(&linear_tc_kernel<TFX_BITS>);
   k.decode = reinterpret_cast<const void*>(&decode_kernel<TFX_BITS>);
+  k.decode_rate = reinterpret_cast<const void*>(&decode_rate_kernel<TFX_BITS>);
   return k;
 }
 

@@ -4,10 +4,12 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "../../include/tfx_exl3.h"
@@ -103,7 +105,14 @@ int rt_alloc(void** p, size_t bytes, cudaStream_t s) { return cudaMallocAsync(p,
 int rt_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s) == cudaSuccess ? 0 : -1; }
 int rt_memset0(void* p, size_t bytes, cudaStream_t s) { return cudaMemsetAsync(p, 0, bytes, s) == cudaSuccess ? 0 : -1; }
 
-tfx_exl3_driver g_drv = {rt_alloc, rt_free, rt_memset0};
+// Allocation hooks of reserve/release (the CUDA runtime, or a test's fake);
+// swapped and read under a lock so that a test hook never tears a call.
+std::mutex g_drv_mu;
+tfx_exl3_driver g_drv_hooks = {rt_alloc, rt_free, rt_memset0};
+tfx_exl3_driver drv() {
+  std::lock_guard<std::mutex> lk(g_drv_mu);
+  return g_drv_hooks;
+}
 
 int env_variant() {
   const char* v = getenv("TFX_EXL3_VARIANT");
@@ -121,9 +130,11 @@ int env_pdl() {
   const char* v = getenv("TFX_EXL3_PDL");
   return v && !strcmp(v, "1");
 }
-int g_variant = env_variant();
+// Process-wide switches: read by every call, written by the set_* hooks.
+std::atomic<int> g_variant{env_variant()};
 thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
-int g_pdl = env_pdl();
+std::atomic<int> g_pdl{env_pdl()};
+std::atomic<long long> g_spin{tfx::kSpinClocks};
 
 // ---------------------------------------------------------------- per-weight state
 
@@ -193,10 +204,9 @@ int rows_group(int TN, int C, int rows) {
   return g;
 }
 
-const tfx::KernelSet& kernels(int bits) {
-  static tfx::KernelSet ks[9];
-  static bool init = false;
-  if (!init) {
+struct KernelTable {
+  tfx::KernelSet ks[9];
+  KernelTable() {
     ks[1] = tfx::kernels_b1();
     ks[2] = tfx::kernels_b2();
     ks[3] = tfx::kernels_b3();
@@ -205,9 +215,12 @@ const tfx::KernelSet& kernels(int bits) {
     ks[6] = tfx::kernels_b6();
     ks[7] = tfx::kernels_b7();
     ks[8] = tfx::kernels_b8();
-    init = true;
   }
-  return ks[bits];
+};
+// Built once, on first use (a function-local static: thread-safe initialisation).
+const tfx::KernelSet& kernels(int bits) {
+  static const KernelTable table;
+  return table.ks[bits];
 }
 
 // Launch with an optional programmatic dependency on the previous kernel of
@@ -273,7 +286,7 @@ Family pick(int bits, int rows) {
   const Family warpk{ks.linear_warp[i], tfx::warp_cta_warps(ncol), ncol, kRowsWarp, 1 << i};
   const Family rowsk{ks.linear_rows[i], tfx::kRowsTC * tfx::kRowsGW, 1, kRowsCta, 1 << i};
   const Family tc{ks.linear_tc, tfx::kTcThreads / 32, 0, kTensor, 0};
-  switch (g_variant) {
+  switch (g_variant.load(std::memory_order_relaxed)) {
     case 1: return rows <= tfx::kRowsMaxRows ? rowsk : tc;
     case 2: return tc;
     case 3: return rows <= tfx::kRowsMaxRows ? warpk : tc;
@@ -464,7 +477,9 @@ cudaError_t record_event(cudaEvent_t e, cudaStream_t s) {
 }
 
 // Validation of a call; on success every member is well formed and aligned.
-int validate_call(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[]) {
+// ldy / col0 (either may be null: N and 0) give each member's output window.
+int validate_call(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
+                  const int64_t* ldy, const int* col0) {
   if (count < 1 || count > 3) return fail(TFX_EINVAL, "group count %d outside 1..3", count);
   if (rows < 0) return fail(TFX_EINVAL, "rows=%d", rows);
   if (!x || !ys) return fail(TFX_EINVAL, "null x or ys");
@@ -475,13 +490,21 @@ int validate_call(tfx_exl3_weight* const ws[], int count, const void* x, int row
     if (!aligned16(ys[i])) return fail(TFX_EALIGN, "y of member %d is not 16-byte aligned", i);
     if (ws[i]->K != ws[0]->K || ws[i]->bits != ws[0]->bits || ws[i]->act != ws[0]->act)
       return fail(TFX_EUNSUPPORTED, "group members must share K, bits and act");
+    const int c0 = col0 ? col0[i] : 0;
+    const long long ld = ldy ? ldy[i] : ws[i]->N;
+    if (c0 < 0 || c0 >= ws[i]->N || c0 % 8)
+      return fail(TFX_EINVAL, "col0=%d of member %d: a multiple of 8 in [0, N=%d)", c0, i, ws[i]->N);
+    if (ld < ws[i]->N - c0 || ld % 8)
+      return fail(TFX_EINVAL, "ldy=%lld of member %d: a multiple of 8 and at least N - col0 = %d", ld, i,
+                  ws[i]->N - c0);
   }
   if (!aligned16(x)) return fail(TFX_EALIGN, "x is not 16-byte aligned");
   return 0;
 }
 
-int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s) {
-  int rc = validate_call(ws, count, x, rows, ys);
+int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], const int64_t* ldy,
+        const int* col0, cudaStream_t s) {
+  int rc = validate_call(ws, count, x, rows, ys, ldy, col0);
   if (rc) return rc;
   if (rows == 0) return 0;
   tfx::Scratch sc = {};
@@ -495,19 +518,20 @@ int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* c
     sc.counters[i] = pv->counters + tfx::kErrorInts;
     if (i == 0) sc.err = pv->counters;
   }
-  return tfx::launch_layer(ws, count, x, rows, ys, s, sc, g_pdl != 0);
+  return tfx::launch_layer(ws, count, x, rows, ys, ldy, col0, s, sc, g_pdl.load(std::memory_order_relaxed) != 0);
 }
 
 int grow(void** p, size_t* have, size_t want, cudaStream_t s, Priv* pv, bool zero) {
   if (want <= *have) return 0;
   void* np = nullptr;
-  if (g_drv.alloc(&np, want, s) != 0 || !np) return fail(TFX_ECUDA, "allocation of %zu bytes failed", want);
+  const tfx_exl3_driver d = drv();
+  if (d.alloc(&np, want, s) != 0 || !np) return fail(TFX_ECUDA, "allocation of %zu bytes failed", want);
   pv->allocs++;
   if (zero) {
-    if (g_drv.memset0(np, want, s) != 0) return fail(TFX_ECUDA, "zeroing %zu bytes failed", want);
+    if (d.memset0(np, want, s) != 0) return fail(TFX_ECUDA, "zeroing %zu bytes failed", want);
     pv->memsets++;
   }
-  if (*p) g_drv.free(*p, s);
+  if (*p) d.free(*p, s);
   *p = np;
   *have = want;
   return 0;
@@ -546,8 +570,9 @@ size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
     const size_t m = (size_t)(C / rows_gw(C)) * mid * w->N * 4;
     need = m > need ? m : need;
   }
-  // tensor-core slabs: one pass of at most kTcRowsMax rows, at most C slabs
-  // (calls above kTcRowsMax rows keep every chunk in one unit and write none)
+  // tensor-core slabs: one pass of at most kTcRowsMax rows, at most C slabs;
+  // calls above kTcRowsMax rows keep every chunk in one unit and write none,
+  // so a reserve for more rows needs no more than one for kTcRowsMax rows
   const int rp = rows < kTcRowsMax ? rows : kTcRowsMax;
   const size_t tc = (size_t)C * rp * w->N * 4;
   return tc > need ? tc : need;
@@ -557,8 +582,8 @@ size_t counter_bytes_needed(const tfx_exl3_weight* w, int rows) {
   return (size_t)(kErrorInts + tc_passes(rows) * (w->N / 128)) * sizeof(int);
 }
 
-int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s,
-                 const Scratch& sc, bool pdl) {
+int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
+                 const int64_t* ldy, const int* col0, cudaStream_t s, const Scratch& sc, bool pdl) {
   const int K = ws[0]->K, bits = ws[0]->bits;
 
   // rotation of x, once for all members
@@ -593,6 +618,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   la.rp = rows < per_pass ? rows : per_pass;
   la.act = ws[0]->act;
   la.err = sc.err;
+  la.spin = g_spin.load(std::memory_order_relaxed);
   long long ctas = 0;
   int tcG = 0;
   if (f.kind == kTensor) {
@@ -609,6 +635,8 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     m.suh = reinterpret_cast<const __half*>(w->suh);
     m.xf = sc.xf[i];
     m.y = ys[i];
+    m.ldy = ldy ? ldy[i] : w->N;
+    m.col0 = col0 ? col0[i] : 0;
     m.partial = sc.partial[i];
     m.counters = sc.counters[i];
     m.N = w->N;
@@ -724,13 +752,20 @@ extern "C" {
 int tfx_exl3_linear(tfx_exl3_weight* w, const void* x, int rows, void* y, cudaStream_t stream) {
   tfx_exl3_weight* ws[1] = {w};
   void* ys[1] = {y};
-  return run(ws, 1, x, rows, ys, stream);
+  return run(ws, 1, x, rows, ys, nullptr, nullptr, stream);
 }
 
 int tfx_exl3_group(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
                    cudaStream_t stream) {
   if (!ws) return fail(TFX_EINVAL, "null member list");
-  return run(ws, count, x, rows, ys, stream);
+  return run(ws, count, x, rows, ys, nullptr, nullptr, stream);
+}
+
+int tfx_exl3_group_into(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
+                        const int64_t ldy[], const int col0[], cudaStream_t stream) {
+  if (!ws) return fail(TFX_EINVAL, "null member list");
+  if (!ldy || !col0) return fail(TFX_EINVAL, "null ldy or col0");
+  return run(ws, count, x, rows, ys, ldy, col0, stream);
 }
 
 int tfx_exl3_columns(const tfx_exl3_weight* w, int from, int n, tfx_exl3_weight* view_out) {
@@ -774,11 +809,12 @@ int tfx_exl3_release(tfx_exl3_weight* w) {
   if (!w) return fail(TFX_EINVAL, "null weight");
   Priv* pv = static_cast<Priv*>(w->priv);
   if (!pv) return 0;
-  if (g_drv.alloc == rt_alloc) cudaDeviceSynchronize();
-  if (pv->xf) g_drv.free(pv->xf, nullptr);
-  if (pv->partial) g_drv.free(pv->partial, nullptr);
-  if (pv->counters) g_drv.free(pv->counters, nullptr);
-  if (g_drv.alloc == rt_alloc) cudaDeviceSynchronize();
+  const tfx_exl3_driver d = drv();
+  if (d.alloc == rt_alloc) cudaDeviceSynchronize();
+  if (pv->xf) d.free(pv->xf, nullptr);
+  if (pv->partial) d.free(pv->partial, nullptr);
+  if (pv->counters) d.free(pv->counters, nullptr);
+  if (d.alloc == rt_alloc) cudaDeviceSynchronize();
   delete pv;
   w->priv = nullptr;
   return 0;
@@ -788,7 +824,7 @@ int tfx_exl3_reset_counters(tfx_exl3_weight* w, cudaStream_t stream) {
   if (!w) return fail(TFX_EINVAL, "null weight");
   Priv* pv = static_cast<Priv*>(w->priv);
   if (!pv || !pv->counters) return fail(TFX_ENOTRESERVED, "weight not reserved");
-  if (g_drv.memset0(pv->counters, pv->counter_bytes, stream) != 0) return fail(TFX_ECUDA, "zeroing counters");
+  if (drv().memset0(pv->counters, pv->counter_bytes, stream) != 0) return fail(TFX_ECUDA, "zeroing counters");
   pv->memsets++;
   return 0;
 }
@@ -838,25 +874,38 @@ int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets) 
 }
 
 int tfx_exl3_set_variant(int variant) {
-  const int old = g_variant;
-  if (variant >= 0 && variant <= 3) g_variant = variant;
-  return old;
+  if (variant < 0 || variant > 3) return g_variant.load();
+  return g_variant.exchange(variant);
 }
 
-int tfx_exl3_set_pdl(int on) {
-  const int old = g_pdl;
-  g_pdl = on ? 1 : 0;
-  return old;
+int tfx_exl3_set_pdl(int on) { return g_pdl.exchange(on ? 1 : 0); }
+
+int64_t tfx_exl3_debug_set_spin_limit(int64_t clocks) {
+  return g_spin.exchange(clocks > 0 ? clocks : tfx::kSpinClocks);
 }
 
 int tfx_exl3_debug_set_driver(const tfx_exl3_driver* d) {
+  std::lock_guard<std::mutex> lk(g_drv_mu);
   if (!d) {
-    g_drv = tfx_exl3_driver{rt_alloc, rt_free, rt_memset0};
+    g_drv_hooks = tfx_exl3_driver{rt_alloc, rt_free, rt_memset0};
     return 0;
   }
   if (!d->alloc || !d->free || !d->memset0) return fail(TFX_EINVAL, "driver hooks must all be set");
-  g_drv = *d;
+  g_drv_hooks = *d;
   return 0;
+}
+
+int tfx_exl3_debug_decode_rate(int bits, int tiles_per_warp, float* sink, int* sink_floats, int64_t* weights,
+                               cudaStream_t stream) {
+  if (bits < 1 || bits > 8 || tiles_per_warp < 1 || !sink_floats || !weights)
+    return fail(TFX_EINVAL, "debug_decode_rate: bits 1..8, tiles_per_warp >= 1, non-null sink_floats and weights");
+  const int ctas = sm_count() * tfx::kRateCtasPerSm;
+  *sink_floats = ctas * tfx::kRateWarps;
+  *weights = (int64_t)ctas * tfx::kRateWarps * tiles_per_warp * 256;
+  if (!sink) return 0;
+  if (!aligned16(sink)) return fail(TFX_EALIGN, "sink must be 16-byte aligned");
+  tfx::RateArgs ra{tiles_per_warp, sink};
+  return launch(kernels(bits).decode_rate, dim3((unsigned)ctas), dim3(tfx::kRateWarps * 32), 0, stream, &ra, false);
 }
 
 int tfx_exl3_debug_error(const tfx_exl3_weight* w, int* device_error) {

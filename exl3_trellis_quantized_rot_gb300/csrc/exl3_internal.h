@@ -27,9 +27,10 @@ int chunks_of(int K);
 size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows);
 size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows);
 size_t counter_bytes_needed(const tfx_exl3_weight* w, int rows);
-// Enqueue the rotation and the linear launch for validated members on `s`.
-int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[], cudaStream_t s,
-                 const Scratch& sc, bool pdl);
+// Enqueue the rotation and the linear launch for validated members on `s`;
+// ldy / col0 give each member's output window (null: N and 0).
+int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
+                 const int64_t* ldy, const int* col0, cudaStream_t s, const Scratch& sc, bool pdl);
 int report_error(int code, const char* msg);
 
 }  // namespace tfx

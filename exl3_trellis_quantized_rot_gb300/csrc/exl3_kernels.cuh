@@ -60,7 +60,9 @@ struct Member {
   const __half* svh;        // N
   const __half* suh;        // K (read by the decode-rows kernel when it rotates x itself)
   const uint2* xf;          // rotated x in B-fragment order (see xf_index)
-  void* y;                  // rows x N, act dtype
+  void* y;                  // output: element (r, n) at y + r*ldy + (n - col0), act dtype
+  long long ldy;            // elements between output rows (N for a plain call)
+  int col0;                 // first output column stored (0 for a plain call; a multiple of 8)
   float* partial;           // [pass][P][rp][N] FP32 subtree sums
   int* counters;            // [pass][NB]
   int N, NB;
@@ -82,6 +84,7 @@ struct LinearArgs {
   int act;      // 0 FP16, 1 BF16
   long long items;  // work items of the warp-granular kernel (all members)
   int* err;         // device error word of the call
+  long long spin;   // clock cycles a bounded wait polls before it gives up
   int box_rows;     // warp-granular kernel: tile rows per tensor copy of trellis words (H)
   int ring_boxes;   // warp-granular kernel: trellis copies in flight per warp (R, 1 or 2)
   int x_rows;       // warp-granular kernel: tile rows per x stage (the whole chunk, or H)
@@ -212,6 +215,36 @@ __device__ __forceinline__ float tree_load(const float* p, long long stride, int
   return tree_sum<16>(v);
 }
 
+// Output columns n0 .. n0+3 (n0 a multiple of 4) of row r of member M, rounded
+// to the output dtype. Element (r, n) sits at M.y + r*M.ldy + (n - M.col0);
+// columns below M.col0 are not stored (col0 is a multiple of 8, so the four
+// columns are kept or dropped together).
+__device__ __forceinline__ void store_y4(const Member& M, int act, long long r, int n0, const float (&v)[4]) {
+  if (n0 < M.col0) return;
+  const long long yo = r * M.ldy + (n0 - M.col0);
+  uint2 out;
+  if (act == 0) {
+    __half2 o0 = __floats2half2_rn(v[0], v[1]), o1 = __floats2half2_rn(v[2], v[3]);
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(M.y) + yo) = out;
+  } else {
+    __nv_bfloat162 o0 = __floats2bfloat162_rn(v[0], v[1]), o1 = __floats2bfloat162_rn(v[2], v[3]);
+    out.x = *reinterpret_cast<uint32_t*>(&o0);
+    out.y = *reinterpret_cast<uint32_t*>(&o1);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(M.y) + yo) = out;
+  }
+}
+// One output element (r, n) of member M (dropped below M.col0).
+__device__ __forceinline__ void store_y1(const Member& M, int act, long long r, int n, float v) {
+  if (n < M.col0) return;
+  const long long yo = r * M.ldy + (n - M.col0);
+  if (act == 0)
+    reinterpret_cast<__half*>(M.y)[yo] = __float2half_rn(v);
+  else
+    reinterpret_cast<__nv_bfloat16*>(M.y)[yo] = __float2bfloat16_rn(v);
+}
+
 // Unnormalised 128-point Walsh-Hadamard transform (Sylvester order) of the
 // 128 values a warp holds, 4 per lane (element 4*lane + e). Fixed butterfly
 // order: strides 1, 2 in-thread, then 4..64 across lanes.
@@ -321,19 +354,7 @@ __device__ __forceinline__ void combine_item(const LinearArgs& a, const Member& 
   for (int e = 0; e < 4; e++) sv[e] = __half2float(M.svh[n0 + e]);
 #pragma unroll
   for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
-  const long long yo = (long long)r * M.N + n0;
-  uint2 out;
-  if (a.act == 0) {
-    __half2 o0 = __floats2half2_rn(v[0], v[1]), o1 = __floats2half2_rn(v[2], v[3]);
-    out.x = *reinterpret_cast<uint32_t*>(&o0);
-    out.y = *reinterpret_cast<uint32_t*>(&o1);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(M.y) + yo) = out;
-  } else {
-    __nv_bfloat162 o0 = __floats2bfloat162_rn(v[0], v[1]), o1 = __floats2bfloat162_rn(v[2], v[3]);
-    out.x = *reinterpret_cast<uint32_t*>(&o0);
-    out.y = *reinterpret_cast<uint32_t*>(&o1);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(M.y) + yo) = out;
-  }
+  store_y4(M, a.act, r, n0, v);
 }
 
 // Words of one tile a lane needs: its 8 weights' windows span bits
@@ -448,19 +469,7 @@ __device__ __forceinline__ void block_epilogue(const Member& M, const LinearArgs
     fwht128(v, lane);
 #pragma unroll
     for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
-    const long long yo = (long long)(row0 + r) * M.N + n0;
-    uint2 out;
-    if (a.act == 0) {
-      __half2 o0 = __floats2half2_rn(v[0], v[1]), o1 = __floats2half2_rn(v[2], v[3]);
-      out.x = *reinterpret_cast<uint32_t*>(&o0);
-      out.y = *reinterpret_cast<uint32_t*>(&o1);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(M.y) + yo) = out;
-    } else {
-      __nv_bfloat162 o0 = __floats2bfloat162_rn(v[0], v[1]), o1 = __floats2bfloat162_rn(v[2], v[3]);
-      out.x = *reinterpret_cast<uint32_t*>(&o0);
-      out.y = *reinterpret_cast<uint32_t*>(&o1);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(M.y) + yo) = out;
-    }
+    store_y4(M, a.act, row0 + r, n0, v);
   }
 }
 
@@ -693,7 +702,7 @@ __global__ void __launch_bounds__(kRowsTC * kRowsGW * 32, MINB)
 // order), rotates back (FWHT, 1/sqrt(128)), scales by svh and stores y. A
 // second cluster barrier keeps every CTA's shared memory alive until all
 // reads are done. No scratch, no counters, no second kernel.
-constexpr long long kSpinClocks = 2000000000LL;  // clock cycles before a wait gives up (about 1 s)
+constexpr long long kSpinClocks = 2000000000LL;  // default clock cycles before a wait gives up (about 1 s)
 
 // try_wait with a suspend-time hint: a thread whose phase is not complete is
 // descheduled until it completes or about `ns` nanoseconds pass, so waiting
@@ -708,16 +717,17 @@ __device__ __forceinline__ bool mbar_test_sleep(uint64_t* b, uint32_t parity, ui
   return ok != 0;
 }
 
-// Wait for the phase of the given parity, at most kSpinClocks; false on a
-// timeout. The wait spins on the non-blocking test: measured on GB300, a
-// try_wait that finds the phase incomplete suspends the thread for a fixed
-// slice (about half a microsecond) rather than until the phase completes,
-// which made every producer/consumer hand-off cost that much.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity) {
+// Wait for the phase of the given parity, at most `spin` clock cycles (the
+// launch's limit, kSpinClocks unless a test lowers it); false on a timeout.
+// The wait spins on the non-blocking test: measured on GB300, a try_wait
+// that finds the phase incomplete suspends the thread for a fixed slice
+// (about half a microsecond) rather than until the phase completes, which
+// made every producer/consumer hand-off cost that much.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity, long long spin) {
   if (mbar_poll(b, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_poll(b, parity))
-    if (clock64() - t0 > kSpinClocks) return false;
+    if (clock64() - t0 > spin) return false;
   return true;
 }
 
@@ -767,7 +777,8 @@ __device__ __forceinline__ void cluster_fold(const float* local, float (&v)[4]) 
 // values (4 per lane), x 1/sqrt(128), x svh, round to the output dtype.
 // sv4 holds the lane's 4 svh values (read before the caller's barriers, so
 // that no global load sits on the epilogue's critical path).
-__device__ __forceinline__ void rot_out_row(float (&v)[4], uint2 sv4, void* y, long long yo, int act, int lane) {
+__device__ __forceinline__ void rot_out_row(float (&v)[4], uint2 sv4, const Member& M, long long r, int n0, int act,
+                                            int lane) {
   fwht128(v, lane);
   float sv[4];
   {
@@ -779,18 +790,7 @@ __device__ __forceinline__ void rot_out_row(float (&v)[4], uint2 sv4, void* y, l
   }
 #pragma unroll
   for (int e = 0; e < 4; e++) v[e] = (v[e] * kInvSqrt128) * sv[e];
-  uint2 out;
-  if (act == 0) {
-    __half2 o0 = __floats2half2_rn(v[0], v[1]), o1 = __floats2half2_rn(v[2], v[3]);
-    out.x = *reinterpret_cast<uint32_t*>(&o0);
-    out.y = *reinterpret_cast<uint32_t*>(&o1);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(y) + yo) = out;
-  } else {
-    __nv_bfloat162 o0 = __floats2bfloat162_rn(v[0], v[1]), o1 = __floats2bfloat162_rn(v[2], v[3]);
-    out.x = *reinterpret_cast<uint32_t*>(&o0);
-    out.y = *reinterpret_cast<uint32_t*>(&o1);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(y) + yo) = out;
-  }
+  store_y4(M, act, r, n0, v);
 }
 
 // Shared memory of the warp-granular kernel: R stages of x (NR row groups x H
@@ -929,8 +929,8 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
   for (int b = 0; b < nbox && alive; b++) {
     const int st = b & (R - 1);
     const uint32_t par = (uint32_t)(b / R) & 1u;
-    bool ok = mbar_wait_bounded(&wfull[warp][st], par);
-    if (!fuse && (xw ? b == 0 : true)) ok = ok && mbar_wait_bounded(&xfull[xw ? 0 : st], xw ? 0u : par);
+    bool ok = mbar_wait_bounded(&wfull[warp][st], par, a.spin);
+    if (!fuse && (xw ? b == 0 : true)) ok = ok && mbar_wait_bounded(&xfull[xw ? 0 : st], xw ? 0u : par, a.spin);
     if (!__all_sync(0xffffffffu, ok)) {
       alive = false;
       break;
@@ -971,7 +971,7 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
         if (!xw) {
           mbar_arrive(&xempty[st]);
           if (warp == 0) {
-            if (mbar_wait_bounded(&xempty[st], par))
+            if (mbar_wait_bounded(&xempty[st], par, a.spin))
               load_x(b + R);
             else
               s_dead = 1;
@@ -1029,7 +1029,7 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
       case 8: cluster_fold<8>(src, v); break;
       default: cluster_fold<16>(src, v); break;
     }
-    rot_out_row(v, sv4, M.y, (long long)r * M.N + nb * 128 + 4 * lane, a.act, lane);
+    rot_out_row(v, sv4, M, r, nb * 128 + 4 * lane, a.act, lane);
   }
   cluster_sync();
 }
@@ -1061,12 +1061,51 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ Dec
   }
 }
 
+// Decode-rate probe: the decode rule's arithmetic at full occupancy with no
+// global-memory traffic. Each warp decodes `tiles` tiles whose words it reads
+// from a table of 64 tiles in shared memory (as the decode-rows kernels read
+// their staged words) and feeds each decoded A fragment to one m16n8k16 MMA;
+// one float per warp goes to `sink` so that nothing is optimised away. Timed
+// by the caller, it gives the decoded weights per second this GPU sustains
+// for the rule: the ALU roofline of the decode-bound calls.
+constexpr int kRateWarps = 8;
+constexpr int kRateCtasPerSm = 8;
+struct RateArgs {
+  int tiles;
+  float* sink;  // gridDim.x * kRateWarps floats
+};
+
+template <int BITS>
+__global__ void __launch_bounds__(kRateWarps * 32) decode_rate_kernel(const __grid_constant__ RateArgs a) {
+  __shared__ uint32_t table[64 * 8 * BITS];
+  for (int i = threadIdx.x; i < 64 * 8 * BITS; i += blockDim.x)
+    table[i] = ((uint32_t)i * 2654435761u) ^ ((uint32_t)blockIdx.x * 40503u);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  LaneWindow<BITS> lw;
+  lw.init(lane);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t xb = 0x3c003c00u;  // FP16 ones
+  for (int t = 0; t < a.tiles; t++) {
+    const uint32_t* tile = table + ((t + warp) & 63) * (8 * BITS);
+    uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
+    raw[0] = tile[lw.i0];
+    raw[1] = tile[lw.i1];
+    if constexpr (Geo<BITS>::kRaw > 2) raw[2] = tile[lw.i2];
+    lw.align(raw, win);
+    decode8<BITS>(win, af);
+    mma16816(acc, af, xb, xb);
+  }
+  if (lane == 0) a.sink[blockIdx.x * kRateWarps + warp] = acc[0] + acc[1] + acc[2] + acc[3];
+}
+
 // Kernel pointers for one bit width (defined in exl3_bits.cu).
 struct KernelSet {
   const void* linear_rows[4];  // decode-rows family: NR = 1, 2, 4, 8 (8, 16, 32, 64 rows)
   const void* linear_warp[4];  // warp-granular decode-rows kernel, same row tiles
   const void* linear_tc;       // tensor-core family: any row count, persistent
   const void* decode;
+  const void* decode_rate;     // decode-rate probe
 };
 
 }  // namespace tfx

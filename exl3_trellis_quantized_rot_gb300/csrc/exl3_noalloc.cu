@@ -13,7 +13,8 @@
 // current) on the first call made on that device. Make that first call before
 // any stream capture. All calls share the one array and see what the last
 // call left there; calls that overlap on the GPU (other streams, other
-// threads) race on it, so order them on one stream.
+// threads) race on it, so order them on one stream. The stream must belong
+// to the current device.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -33,12 +34,20 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_dev_ptr[kMaxDevices] = {};
 
-// Device address of the static scratch on the current device (set up once).
-int scratch_on_current_device(unsigned char** out) {
+// Device address of the static scratch on the current device (set up once),
+// after checking that `stream` belongs to that device.
+int scratch_on_current_device(cudaStream_t stream, unsigned char** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return tfx::report_error(TFX_ECUDA, cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return tfx::report_error(TFX_EUNSUPPORTED, "device ordinal out of range");
+  if (stream) {
+    int sdev = -1;
+    e = cudaStreamGetDevice(stream, &sdev);
+    if (e != cudaSuccess) return tfx::report_error(TFX_ECUDA, cudaGetErrorString(e));
+    if (sdev != dev)
+      return tfx::report_error(TFX_EINVAL, "the stream belongs to another device than the current one");
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_dev_ptr[dev]) {
     void* p = nullptr;
@@ -77,7 +86,7 @@ extern "C" int tfx_exl3_linear_static(const tfx_exl3_weight* w, const void* x, i
     return tfx::report_error(TFX_EUNSUPPORTED, msg);
   }
   unsigned char* base = nullptr;
-  rc = scratch_on_current_device(&base);
+  rc = scratch_on_current_device(stream, &base);
   if (rc) return rc;
   tfx::Scratch sc = {};
   sc.err = reinterpret_cast<int*>(base);
@@ -85,12 +94,14 @@ extern "C" int tfx_exl3_linear_static(const tfx_exl3_weight* w, const void* x, i
   sc.xf[0] = reinterpret_cast<uint2*>(base + kCounterBytes);
   sc.partial[0] = reinterpret_cast<float*>(base + kCounterBytes + align256(xf_bytes));
 
-  // the array keeps whatever the last call left: start this call's counters at zero
-  cudaError_t e = cudaMemsetAsync(sc.counters[0], 0, counter_bytes, stream);
+  // the array keeps whatever the last call left: clear the device error word
+  // and exactly this call's counters (counter_bytes covers both, from the
+  // start of the array)
+  cudaError_t e = cudaMemsetAsync(base, 0, counter_bytes, stream);
   if (e != cudaSuccess) return tfx::report_error(TFX_ECUDA, cudaGetErrorString(e));
 
   tfx_exl3_weight wc = *w;
   tfx_exl3_weight* ws[1] = {&wc};
   void* ys[1] = {y};
-  return tfx::launch_layer(ws, 1, x, rows, ys, stream, sc, false);
+  return tfx::launch_layer(ws, 1, x, rows, ys, nullptr, nullptr, stream, sc, false);
 }

@@ -56,7 +56,6 @@ constexpr int kTcXStage = kTcSK * kTcRowsMax * 32;    // x bytes per stage (32 K
 constexpr int kTcAB = 3;                              // A (decoded weight) buffers
 constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (32 KB)
 constexpr int kTcExBytes = 2 * 4 * 128 * 4;           // epilogue exchange (two 4-row groups)
-constexpr long long kTcSpin = 2000000000LL;  // clock cycles before a wait gives up
 constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcExBytes;
 // named barriers (0 is __syncthreads)
 constexpr int kBarFold = 1;        // the 4 fold warps
@@ -65,20 +64,20 @@ constexpr int kBarFolded = 5;      // + chunk parity: fold warps -> MMA warp (2 
 constexpr int kReadyThreads = (kTcDecodeWarps + 1) * 32;
 constexpr int kFoldedThreads = 5 * 32;
 
-// Wait for the phase of the given parity to complete, at most kTcSpin cycles.
+// Wait for the phase of the given parity to complete, at most `spin` cycles.
 // The thread polls with the non-blocking test (a try_wait on an incomplete
 // phase suspends the thread for a fixed slice instead of until completion),
 // sleeping sleep_ns between polls so that waiting warps leave the issue slots
 // of their scheduler to the warps doing work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
-                                          int sleep_ns = 0) {
+                                          long long spin, int sleep_ns = 0) {
   if (*abort_flag) return false;
   if (mbar_poll(b, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_poll(b, parity)) {
     if (*abort_flag) return false;
     if (sleep_ns) __nanosleep(sleep_ns);
-    if (clock64() - t0 > kTcSpin) {
+    if (clock64() - t0 > spin) {
       *abort_flag = 1;
       atomicExch(err, 1);
       return false;
@@ -222,9 +221,9 @@ __device__ __forceinline__ bool fold_all(bool ok) {
 }
 // One lane polls, the warp follows with a warp-uniform outcome.
 __device__ __forceinline__ bool wait_lane0(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
-                                           int lane, int sleep_ns) {
+                                           long long spin, int lane, int sleep_ns) {
   int ok = 1;
-  if (lane == 0) ok = mbar_wait(b, parity, abort_flag, err, sleep_ns);
+  if (lane == 0) ok = mbar_wait(b, parity, abort_flag, err, spin, sleep_ns);
   ok = __shfl_sync(0xffffffffu, ok, 0);
   return ok != 0;
 }
@@ -233,8 +232,8 @@ __device__ __forceinline__ bool wait_lane0(uint64_t* b, uint32_t parity, volatil
 // of the four fold warps: finish the Walsh-Hadamard transform over n in the
 // same stage order as fwht128 (n bits 0..4 across lanes, then bits 5 and 6
 // through shared memory), scale by 1/sqrt(128) and svh, store y.
-__device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane, float* ex, float sv, void* y,
-                                                 long long yrow0, int N, int nrows, int act) {
+__device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane, float* ex, float sv, const Member& M,
+                                                 long long row0, int ncol, int nrows, int act) {
 #pragma unroll
   for (int m = 0; m < 5; m++) {
     const bool hi = (lane >> m) & 1;
@@ -255,13 +254,7 @@ __device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane,
     const float u1 = h5 ? (c - b) : (b + c);
     float o = (n & 64) ? (u1 - u0) : (u0 + u1);
     o = (o * kInvSqrt128) * sv;
-    if (e < nrows) {
-      const long long yo = yrow0 + (long long)e * N;
-      if (act == 0)
-        reinterpret_cast<__half*>(y)[yo] = __float2half_rn(o);
-      else
-        reinterpret_cast<__nv_bfloat16*>(y)[yo] = __float2bfloat16_rn(o);
-    }
+    if (e < nrows) store_y1(M, act, row0 + e, ncol, o);
   }
 }
 
@@ -373,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           const int ab = gs % kTcAB;
           // buffer ab last held stage gs - kTcAB: wait until its MMAs completed
           if (gs >= kTcAB) {
-            if (lane == 0) mbar_wait(&sdone[ab], ((gs - kTcAB) / kTcAB) & 1, &s_abort, ta.err);
+            if (lane == 0) mbar_wait(&sdone[ab], ((gs - kTcAB) / kTcAB) & 1, &s_abort, ta.err, a.spin);
             __syncwarp();
           }
           if (!s_abort) {
@@ -412,7 +405,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
       const long long slab = (long long)a.rp * M.N;
       for (int c = 0; c < M.G; c++) {
         gc++;
-        const bool ok = fold_all(wait_lane0(&chunk_done[gc & 1], (gc >> 1) & 1, &s_abort, ta.err, lane, 64));
+        const bool ok = fold_all(wait_lane0(&chunk_done[gc & 1], (gc >> 1) & 1, &s_abort, ta.err, a.spin, lane, 64));
         if (ok) {
           tc_fence_after();
           const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * NMf);
@@ -435,9 +428,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
 #pragma unroll
               for (int q = 0; q < 4; q++) {
                 float v4[4] = {v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]};
-                tc_rot_out_store(v4, n, lane, sEx + (exb & 1) * 512, sv, M.y,
-                                 (long long)(U.row0 + cc + 4 * q) * M.N + U.nb * 128 + n, M.N, U.prow - cc - 4 * q,
-                                 a.act);
+                tc_rot_out_store(v4, n, lane, sEx + (exb & 1) * 512, sv, M, U.row0 + cc + 4 * q, U.nb * 128 + n,
+                                 U.prow - cc - 4 * q, a.act);
                 exb++;
               }
             } else {
@@ -470,7 +462,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         const int ab = gs % kTcAB, xs = gs % kTcXS;
         bar_sync(kBarReady + ab, kReadyThreads);
         int okx = 1;
-        if (lane == 0) okx = mbar_wait(&xfull[xs], (gs / kTcXS) & 1, &s_abort, ta.err);
+        if (lane == 0) okx = mbar_wait(&xfull[xs], (gs / kTcXS) & 1, &s_abort, ta.err, a.spin);
         okx = __shfl_sync(0xffffffffu, okx, 0);
         tc_fence_after();
         const bool go = okx && !s_abort;
@@ -530,7 +522,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           const int cnt = min(kTcSK, U.nsteps - s0);
           const int xs = gs % kTcXS;
           int ok = 1;
-          if (lane == 0 && gs >= kTcXS) ok = mbar_wait(&sdone[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, 32);
+          if (lane == 0 && gs >= kTcXS) ok = mbar_wait(&sdone[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, a.spin, 32);
           ok = __shfl_sync(kMask, ok, 0);
           if (!ok || s_abort) continue;
           // bytes = cnt * NMp * 32 is a multiple of 512: every slice is a multiple of 16 bytes

@@ -80,6 +80,21 @@ int tfx_exl3_linear(tfx_exl3_weight* w, const void* x, int rows, void* y, cudaSt
 int tfx_exl3_group(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
                    cudaStream_t stream);
 
+/* tfx_exl3_group with an output window per member: member i's output element
+ * (r, n) is written at ys[i] + r*ldy[i] + (n - col0[i]) (elements of w->act),
+ * for n >= col0[i]; columns below col0[i] are computed but not stored.
+ * col0[i]: a multiple of 8 in [0, N); ldy[i]: a multiple of 8, >= N - col0[i].
+ * Bytes of every stored element equal those of tfx_exl3_linear on the member.
+ * This packs several column views of one weight into one buffer in one call:
+ * the drafter's LM head over two vocabulary spans (PR #1507, "What this
+ * changes": the head() arm computes the views [0, 98304) and the last 64
+ * blocks and packs them into one logits buffer with a 2-D copy that drops the
+ * first 7,904 columns of the tail) is group_into over the two views with
+ * ldy = 98304 + 288, col0 = {0, 7904}, ys = {logits, logits + 98304}: the
+ * epilogue writes the packed layout directly, with no copy. */
+int tfx_exl3_group_into(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
+                        const int64_t ldy[], const int col0[], cudaStream_t stream);
+
 /* A view of whole 128-column blocks [from, from+n) of w that reads the same
  * stored words and keeps the parent's tile-row stride (PR #1507, "What this
  * changes": exl3.Weight.columns(from, n)). from % 128 == 0, n % 128 == 0,
@@ -95,13 +110,17 @@ int tfx_exl3_columns(const tfx_exl3_weight* w, int from, int n, tfx_exl3_weight*
  * where allocation is forbidden, plugins whose host application owns all
  * device memory, runtimes that must not allocate after start-up).
  * w needs no reserve() (w->priv is ignored); x, y as for tfx_exl3_linear.
+ * `stream` must belong to the current device (TFX_EINVAL otherwise).
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture. Each call
- * zeroes the counters it uses with cudaMemsetAsync on `stream` (the array
- * keeps what the previous call left). All calls share the one array: calls
- * that overlap on the GPU race, so order them on one stream. A call whose
- * scratch (counters + rows*K*2 + splits*min(rows,128)*N*4 bytes, rounded)
- * exceeds the array returns TFX_EUNSUPPORTED with the sizes in the message. */
+ * clears the array's device error word and the counters it uses with one
+ * cudaMemsetAsync on `stream` (the array keeps what the previous call left).
+ * The device error word cannot be read through tfx_exl3_debug_error (which
+ * needs a reserved weight): a static call cannot report a bounded wait that
+ * gave up. All calls share the one array: calls that overlap on the GPU race,
+ * so order them on one stream. A call whose scratch (counters + rows*K*2 +
+ * splits*min(rows,128)*N*4 bytes, rounded) exceeds the array returns
+ * TFX_EUNSUPPORTED with the sizes in the message. */
 int tfx_exl3_linear_static(const tfx_exl3_weight* w, const void* x, int rows, void* y, cudaStream_t stream);
 
 /* Size the weight's scratch (rotated x, split-K partials, counters) for up
@@ -169,12 +188,35 @@ typedef struct {
 } tfx_exl3_driver;
 int tfx_exl3_debug_set_driver(const tfx_exl3_driver* d);
 
-/* Device error word of a reserved weight: 1 once a tensor-core launch on it
- * gave up a bounded wait (a broken pipeline, never expected), 2 if it was
- * launched with less shared memory than it lays out (it then does nothing),
- * 0 otherwise. Synchronous copy; for tests and diagnostics. reset_counters
- * clears it. */
+/* Device error word of a reserved weight, written by a launch on it: 1 once
+ * a tensor-core launch gave up a bounded wait (its pipeline stopped; the
+ * launch skips its remaining work and stores nothing more), 2 if a tensor-core
+ * launch got less shared memory than it lays out (it then does nothing), 3
+ * once a decode-rows (warp-granular) launch gave up waiting for a copy of
+ * trellis words or x into shared memory (its CTA stores nothing), 0
+ * otherwise. A wait gives up after the spin limit (about 1 s by default, see
+ * tfx_exl3_debug_set_spin_limit); it is never expected on a healthy GPU.
+ * Synchronous copy; for tests and diagnostics. reset_counters clears it. */
 int tfx_exl3_debug_error(const tfx_exl3_weight* w, int* device_error);
+
+/* Test hook: the clock cycles a bounded wait inside a kernel polls before it
+ * gives up (default 2e9, about 1 s); clocks <= 0 restores the default.
+ * Applies to launches enqueued after the call. Returns the previous limit.
+ * A test lowers it to a few cycles so that waits give up on a healthy GPU and
+ * the error path (device error word, reset_counters, a correct next call) can
+ * be checked without a fault. */
+int64_t tfx_exl3_debug_set_spin_limit(int64_t clocks);
+
+/* Decode-rate probe: launches, on `stream`, the decode rule's arithmetic (one
+ * 16x16 tile decode and one m16n8k16 MMA per step, words read from a table in
+ * shared memory, no global-memory traffic) at full occupancy, tiles_per_warp
+ * tiles per warp, for `bits` 1..8. *weights = weights the launch decodes;
+ * *sink_floats = floats `sink` must hold (one per warp). With sink == NULL
+ * only the two outputs are set and nothing is launched. The caller times the
+ * launch (CUDA events on `stream`): weights / time is the decode rate this GPU
+ * sustains for the rule, the ALU roofline of decode-bound calls. */
+int tfx_exl3_debug_decode_rate(int bits, int tiles_per_warp, float* sink, int* sink_floats, int64_t* weights,
+                               cudaStream_t stream);
 
 /* Measurement hook: the next linear/group call on this thread records
  * `before` just before its linear-kernel launch and `after` just after it,

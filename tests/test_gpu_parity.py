@@ -249,6 +249,60 @@ def test_lm_head_views_equal_full_head():
                          what=f"head rows={rows} blk={blk}")
 
 
+def test_lm_head_span_packing_equals_full_head():
+    """The drafter's head over two vocabulary spans (PR #1507, "What this
+    changes"): the view [0, 98304) and the last 64 blocks, packed into one
+    logits buffer without the tail's first 7,904 columns, in one group_into
+    call; every packed element has the bytes of the same column of the full
+    head."""
+    K, N, bits = 5120, 248320, 6
+    hw, w = make(11, K, N, bits)
+    first = tfx.columns(w, 0, 98304)
+    tail = tfx.columns(w, 240128, 8192)
+    tfx.reserve(first, 16)
+    tfx.reserve(tail, 16)
+    keep = 248320 - 240128 - 7904  # 288 columns of the tail
+    for rows in (1, 8, 16):
+        x64, x = x_of(11, rows, K)
+        full = tfx.linear(w, x)
+        packed = torch.full((rows, 98304 + keep), float("nan"), dtype=torch.float16, device=DEV)
+        tfx.pack_spans([first, tail], x, packed, [0, 7904])
+        assert same_bytes(packed[:, :98304], full[:, :98304])
+        assert same_bytes(packed[:, 98304:], full[:, 240128 + 7904:])
+
+
+@pytest.mark.parametrize("variant", [tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP])
+def test_output_window_bytes_equal_plain_call(variant):
+    # a member's output window (row stride, first stored column) changes where
+    # elements land, never their bytes; columns below col0 and the padding of
+    # each row stay untouched
+    hw, w = make(15, 1024, 768, 4, max_rows=128)
+    hk, k = make(15, 1024, 256, 4, member=1, max_rows=128)
+    tfx.set_variant(variant)
+    try:
+        for rows in (1, 7, 16, 40, 128):
+            x64, x = x_of(15, rows, 1024)
+            ref_w, ref_k = tfx.linear(w, x), tfx.linear(k, x)
+            out = torch.full((rows, 1000), 3.0, dtype=torch.float16, device=DEV)
+            ld = 1000
+            tfx.group_into([w, k], x, [out.data_ptr(), out.data_ptr() + 2 * (768 - 136)], [ld, ld], [136, 8])
+            assert same_bytes(out[:, :768 - 136], ref_w[:, 136:]), rows
+            assert same_bytes(out[:, 768 - 136:768 - 136 + 248], ref_k[:, 8:]), rows
+            assert bool((out[:, 768 - 136 + 248:] == 3.0).all()), rows
+    finally:
+        tfx.set_variant(tfx.VARIANT_AUTO)
+
+
+def test_output_window_validation():
+    hw, w = make(16, 256, 256, 4)
+    x64, x = x_of(16, 1, 256)
+    y = torch.empty((1, 512), dtype=torch.float16, device=DEV)
+    for ld, c0 in ((256, 4), (256, 256), (248, 0), (300, 0), (256, -8)):
+        with pytest.raises(tfx.TfxError) as e:
+            tfx.group_into([w], x, [y], [ld], [c0])
+        assert e.value.code == tfx.EINVAL, (ld, c0)
+
+
 # ------------------------------------------------------------------ edge cases and stress
 
 def test_zero_rows_is_a_no_op():

@@ -255,3 +255,52 @@ def test_kernel_choice_and_tensor_core_unit_size(L):
         with pytest.raises(tfx.TfxError) as e:
             shape(*bad)
         assert e.value.code == tfx.EINVAL, bad
+
+
+def test_output_window_validation_before_any_launch(L, drv):
+    # group_into's window checks run before anything is enqueued
+    w = fake_weight(256, 256, 4)
+    tfx.reserve(w, 4, 0)
+    x = FAKE + (3 << 30)
+    y = FAKE + (4 << 30)
+    arr = (C.POINTER(tfx.WeightStruct) * 1)(C.pointer(w.s))
+    ys = (C.c_void_p * 1)(y)
+    for ld, c0 in ((256, 4), (256, 256), (248, 0), (300, 0), (256, -8), (112, 136)):
+        rc = L.tfx_exl3_group_into(arr, 1, x, 1, ys, (C.c_int64 * 1)(ld), (C.c_int * 1)(c0), None)
+        assert rc == tfx.EINVAL, (ld, c0)
+    assert L.tfx_exl3_group_into(arr, 1, x, 1, ys, None, (C.c_int * 1)(0), None) == tfx.EINVAL
+    # a valid window still needs a reserve large enough
+    rc = L.tfx_exl3_group_into(arr, 1, x, 9, ys, (C.c_int64 * 1)(128), (C.c_int * 1)(128), None)
+    assert rc == tfx.ENOTRESERVED
+
+
+def test_spin_limit_and_decode_rate_query(L):
+    old = tfx.set_spin_limit(7)
+    assert old == 2_000_000_000
+    assert tfx.set_spin_limit(-1) == 7
+    assert tfx.set_spin_limit(0) == 2_000_000_000
+    # the probe's size query launches nothing: 8 CTAs of 8 warps per SM (152
+    # when no device is visible), 256 weights per tile
+    weights, floats = tfx.decode_rate(4, 1000)
+    assert floats % 64 == 0 and weights == floats * 1000 * 256
+    with pytest.raises(tfx.TfxError):
+        tfx.decode_rate(9, 10)
+
+
+def test_switches_are_safe_across_threads(L):
+    import threading
+    old = tfx.set_variant(tfx.VARIANT_AUTO)
+    seen = []
+
+    def flip(v):
+        for _ in range(2000):
+            seen.append(tfx.set_variant(v))
+
+    ts = [threading.Thread(target=flip, args=(v,)) for v in (0, 1, 2, 3)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert set(seen) <= {0, 1, 2, 3}
+    assert tfx.set_variant(9) in (0, 1, 2, 3)  # out of range: unchanged
+    tfx.set_variant(old)
