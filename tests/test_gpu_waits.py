@@ -2,7 +2,9 @@
 
 Every wait of a kernel on a copy into shared memory polls for at most the
 launch's spin limit (about 1 s by default). Lowering the limit to one clock
-cycle makes the first waits give up before the copies land: the CTA then
+cycle makes the first waits give up before the copies land (at 5 or more
+rows: calls of at most 4 rows rotate x inside the kernel, which takes longer
+than the copies of trellis words, so their first poll already succeeds): the CTA then
 records device error 3, waits for its own copies in flight, skips its work
 and still meets its cluster at both barriers, so the launch ends and the
 context stays usable. No fault, trap or endless loop is involved: the copies
@@ -30,7 +32,7 @@ def _lib():
     tfx.set_variant(tfx.VARIANT_AUTO)
 
 
-@pytest.mark.parametrize("rows", [2, 16])
+@pytest.mark.parametrize("rows", [7, 16])
 def test_decode_rows_waits_give_up_and_recover(rows):
     hw, w = make(70, 5120, 1024, 4, max_rows=16)
     x64, x = x_of(70, rows, 5120)
