@@ -493,6 +493,33 @@ def run_gpu(args):
                 lambda i, xr_=xr_, rows=rows: tfx.linear(sets[i % copies][3], xr_, rows, yo[:rows], stream),
                 n_calls), 3)
 
+        # layer chaining: the q/k/v group, then o_proj (K = 6144, N = 5120) on
+        # q's output, at 16 rows: one by one, and as one tfx_exl3_chain with
+        # and without programmatic dependent launch between the kernels
+        o6 = []
+        ocodes = torch.from_numpy(synth.codes(1500 + rank, 6144, O_N, BITS).view(np.int32)).to(dev)
+        osu = torch.from_numpy(synth.suh(1500 + rank, 6144).view(np.int16)).to(dev)
+        osv = torch.from_numpy(synth.svh(1500 + rank, O_N).view(np.int16)).to(dev)
+        for c in range(copies):
+            wc = tfx.Weight(ocodes.clone() if c else ocodes, osu, osv, 6144, O_N, BITS, tfx.F16)
+            tfx.reserve(wc, 128, stream)
+            o6.append(wc)
+        yo6 = torch.empty((ROWS, O_N), dtype=torch.float16, device=dev)
+
+        def unchained(i):
+            q, k, v, _ = sets[i % copies]
+            tfx.group([q, k, v], x, ROWS, ys, stream)
+            tfx.linear(o6[i % copies], ys[0], ROWS, yo6, stream)
+
+        def chained(i, pdl):
+            q, k, v, _ = sets[i % copies]
+            tfx.chain([([q, k, v], x, ys), ([o6[i % copies]], ys[0], [yo6])], ROWS, pdl=pdl, stream=stream)
+
+        detail["chain_qkv_o_rows16_unchained_us"] = round(time_calls(unchained, n_calls), 3)
+        detail["chain_qkv_o_rows16_pdl_off_us"] = round(time_calls(lambda i: chained(i, False), n_calls), 3)
+        detail["chain_qkv_o_rows16_pdl_on_us"] = round(time_calls(lambda i: chained(i, True), n_calls), 3)
+        del o6, ocodes
+
         # mid rows on the 5120x5120 weight (same copies, reserved for 128 rows)
         x128 = torch.from_numpy(synth.activations(2000 + rank, 128, K, "f16")).to(dev)
         y128 = torch.empty((128, O_N), dtype=torch.float16, device=dev)

@@ -26,13 +26,19 @@ ABI_SYMBOLS = ("tfx_exl3_linear", "tfx_exl3_group", "tfx_exl3_columns", "tfx_exl
                "tfx_exl3_stats", "tfx_exl3_set_variant", "tfx_exl3_set_pdl", "tfx_exl3_debug_set_driver",
                "tfx_exl3_debug_mark_events", "tfx_exl3_linear_static", "tfx_exl3_debug_error",
                "tfx_exl3_debug_launch_shape", "tfx_exl3_group_into", "tfx_exl3_debug_set_spin_limit",
-               "tfx_exl3_debug_decode_rate", "tfx_exl3_last_error")
+               "tfx_exl3_debug_decode_rate", "tfx_exl3_chain", "tfx_exl3_encode", "tfx_exl3_encode_scratch_bytes",
+               "tfx_exl3_last_error")
 
 
 class WeightStruct(C.Structure):
     _fields_ = [("trellis", C.c_void_p), ("suh", C.c_void_p), ("svh", C.c_void_p), ("K", C.c_int),
                 ("N", C.c_int), ("bits", C.c_int), ("tile_row_stride", C.c_int64), ("act", C.c_int),
                 ("priv", C.c_void_p)]
+
+
+class StepStruct(C.Structure):
+    _fields_ = [("ws", C.POINTER(C.POINTER(WeightStruct))), ("count", C.c_int), ("x", C.c_void_p),
+                ("ys", C.POINTER(C.c_void_p))]
 
 
 ALLOC_FN = C.CFUNCTYPE(C.c_int, C.POINTER(C.c_void_p), C.c_size_t, C.c_void_p)
@@ -83,6 +89,9 @@ def lib() -> C.CDLL:
                                           C.POINTER(i), vp]
         L.tfx_exl3_debug_set_spin_limit.argtypes = [C.c_int64]
         L.tfx_exl3_debug_decode_rate.argtypes = [i, i, vp, C.POINTER(i), C.POINTER(C.c_int64), vp]
+        L.tfx_exl3_chain.argtypes = [C.POINTER(StepStruct), i, i, i, vp]
+        L.tfx_exl3_encode_scratch_bytes.argtypes = [i, i, i, i, C.POINTER(C.c_size_t)]
+        L.tfx_exl3_encode.argtypes = [vp, i, i, i, vp, vp, vp, C.c_size_t, i, vp]
         L.tfx_exl3_last_error.restype = C.c_char_p
         for n in ABI_SYMBOLS[:-1]:
             getattr(L, n).restype = C.c_int
@@ -234,6 +243,45 @@ def pack_spans(views, x, out, col0, rows: int | None = None, stream=None):
         raise ValueError(f"kept columns {off} != out width {ld}")
     group_into(views, x, ys, [ld] * len(views), list(col0), rows, stream)
     return out
+
+
+def chain(steps, rows: int, pdl: bool = True, stream=None):
+    """Run group calls back to back (tfx_exl3_chain). steps: list of
+    (weights, x, ys); a step's x may be an earlier step's output. Outputs
+    must be allocated by the caller (the chain allocates nothing)."""
+    keep = []
+    arr = (StepStruct * len(steps))()
+    for st, (ws, x, ys) in zip(arr, steps):
+        wa = (C.POINTER(WeightStruct) * len(ws))(*[C.pointer(w.s) for w in ws])
+        ya = (C.c_void_p * len(ys))(*[_ptr(y) for y in ys])
+        keep += [wa, ya]
+        st.ws = C.cast(wa, C.POINTER(C.POINTER(WeightStruct)))
+        st.count = len(ws)
+        st.x = _ptr(x)
+        st.ys = C.cast(ya, C.POINTER(C.c_void_p))
+    _check(lib().tfx_exl3_chain(arr, len(steps), rows, 1 if pdl else 0, _stream(stream)))
+
+
+def encode_scratch_bytes(K: int, N: int, bits: int, max_ctas: int = 0) -> int:
+    n = C.c_size_t()
+    _check(lib().tfx_exl3_encode_scratch_bytes(K, N, bits, max_ctas, C.byref(n)))
+    return n.value
+
+
+def encode(targets, bits: int, max_ctas: int = 0, scratch=None, stream=None):
+    """Trellis words of a K x N weight from int16 grid targets (W*128 rounded),
+    on the GPU. Returns (trellis int32 tensor (K/16, (N/16)*8*bits), per-tile
+    squared error int64 tensor)."""
+    import torch
+    K, N = targets.shape
+    out = torch.empty((K // 16, (N // 16) * 8 * bits), dtype=torch.int32, device=targets.device)
+    err = torch.empty(((K // 16) * (N // 16),), dtype=torch.int64, device=targets.device)
+    need = encode_scratch_bytes(K, N, bits, max_ctas)
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device=targets.device)
+    _check(lib().tfx_exl3_encode(_ptr(targets), K, N, bits, _ptr(out), _ptr(err), _ptr(scratch), scratch.numel(),
+                                 max_ctas, _stream(stream)))
+    return out, err
 
 
 def columns(w: Weight, start: int, n: int) -> Weight:

@@ -38,6 +38,7 @@ def _sources():
             for b in range(1, 9)]
     jobs.append((os.path.join(CSRC, "exl3_host.cu"), os.path.join(OUT, "exl3_host.o"), []))
     jobs.append((os.path.join(CSRC, "exl3_noalloc.cu"), os.path.join(OUT, "exl3_noalloc.o"), []))
+    jobs.append((os.path.join(CSRC, "exl3_encode.cu"), os.path.join(OUT, "exl3_encode.o"), []))
     return deps, jobs
 
 

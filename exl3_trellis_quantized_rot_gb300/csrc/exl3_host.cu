@@ -62,8 +62,8 @@ __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArg
 }
 
 __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ CombineArgs ca) {
-  griddep_launch();
   griddep_wait();
+  griddep_launch();
   const LinearArgs& a = ca.la;
   long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -145,6 +145,8 @@ struct Priv {
   size_t partial_bytes = 0;
   int* counters = nullptr;
   size_t counter_bytes = 0;
+  float* lev = nullptr;  // tensor-core kernel: per-CTA slots for the deepest chunk-tree levels
+  size_t lev_bytes = 0;
   int max_rows = 0;
   int64_t allocs = 0, memsets = 0;
 };
@@ -296,30 +298,40 @@ Family pick(int bits, int rows) {
   }
 }
 
-// Tensor-core kernel: rows per pass, and chunks per work unit (G). Up to 128
-// rows run as one pass; longer calls use 64-row passes so that every unit can
-// hold all C chunks (P = 1, no slabs). Otherwise G is the power of two that
-// minimises the persistent CTAs' critical path, ceil(units / SMs) unit
+// Tensor-core kernel: rows per pass, and chunks per work unit (G). A pass is
+// up to 128 rows (the MMA's N). With level scratch (a reserved weight) every
+// unit of a call above 128 rows holds all C chunks of a 128-row pass: TMEM
+// keeps the two accumulator regions and the first chunk-tree levels, deeper
+// levels go to the scratch, so each weight is decoded once per 128 rows.
+// Without it (the static-scratch entry point) passes above 128 rows are 64
+// rows, where all levels fit in TMEM. Up to 128 rows, G is the power of two
+// that minimises the persistent CTAs' critical path, ceil(units / SMs) unit
 // lengths plus a fixed per-unit cost of 16 k-steps (pipeline fill and fold;
-// measured on GB300 by forcing each G: 5120 x 5120 at 40/64/128 rows best at
-// G = 2, 32.3/33.0/36.0 us against 33.8/34.8/39.6 us at G = 1, which a cost of
-// 8 k-steps chose; the q/k/v group and gate+up keep their G), among those whose
-// TMEM regions fit: (2 + log2 G) * rows columns <= 512. Launch shape only: the
-// bits do not depend on G.
-int tc_rows_per_pass(int rows) { return rows <= tfx::kTcRowsMax ? tfx::kTcRowsMax : tfx::kTcRowsLong; }
-int tc_passes(int rows) {
-  const int rp = tc_rows_per_pass(rows);
+// measured on GB300 by forcing each G), among those whose TMEM regions fit
+// when no level scratch is given. Launch shape only: the bits do not depend
+// on the pass size or on G.
+int tc_rows_per_pass(int rows, bool spill) {
+  return rows <= tfx::kTcRowsMax || spill ? tfx::kTcRowsMax : tfx::kTcRowsNoSpill;
+}
+int tc_passes(int rows, bool spill) {
+  const int rp = tc_rows_per_pass(rows, spill);
   return (rows + rp - 1) / rp;
 }
-int tc_group(long long blocks, int rows, int C, int TK, long long S) {
-  const int passes = tc_passes(rows);
+// Chunk-tree levels a region of nm TMEM columns leaves room for next to the
+// two accumulator regions (at most 4, the levels of 16 chunks).
+int tc_tmem_levels(int nm) {
+  const int l = 512 / nm - 2;
+  return l < tfx::kTcMaxLevels ? l : tfx::kTcMaxLevels;
+}
+int tc_group(long long blocks, int rows, int C, int TK, long long S, bool spill) {
   if (rows > tfx::kTcRowsMax) return C;
   const int nm = (rows + 15) / 16 * 16;
   int best = 1;
   long long best_cost = -1;
   for (int g = C; g >= 1; g /= 2) {
-    if ((2 + __builtin_ctz(g)) * nm > 512) continue;
-    const long long units = blocks * passes * (C / g);
+    const int lg = __builtin_ctz(g);
+    if (lg > tc_tmem_levels(nm) + (spill ? tfx::kTcSpillLevels : 0)) continue;
+    const long long units = blocks * (C / g);
     const long long cost = (units + S - 1) / S * ((long long)TK * g / C + 16);
     if (best_cost < 0 || cost < best_cost) {
       best = g;
@@ -516,7 +528,10 @@ int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* c
     sc.xf[i] = pv->xf;
     sc.partial[i] = pv->partial;
     sc.counters[i] = pv->counters + tfx::kErrorInts;
-    if (i == 0) sc.err = pv->counters;
+    if (i == 0) {
+      sc.err = pv->counters;
+      sc.lev = pv->lev;
+    }
   }
   return tfx::launch_layer(ws, count, x, rows, ys, ldy, col0, s, sc, g_pdl.load(std::memory_order_relaxed) != 0);
 }
@@ -572,14 +587,23 @@ size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
   }
   // tensor-core slabs: one pass of at most kTcRowsMax rows, at most C slabs;
   // calls above kTcRowsMax rows keep every chunk in one unit and write none,
-  // so a reserve for more rows needs no more than one for kTcRowsMax rows
+  // but a weight reserved for more rows also serves calls of up to
+  // kTcRowsMax rows, which may split K into slabs
   const int rp = rows < kTcRowsMax ? rows : kTcRowsMax;
   const size_t tc = (size_t)C * rp * w->N * 4;
   return tc > need ? tc : need;
 }
 
 size_t counter_bytes_needed(const tfx_exl3_weight* w, int rows) {
-  return (size_t)(kErrorInts + tc_passes(rows) * (w->N / 128)) * sizeof(int);
+  // the most passes any call of up to `rows` rows may use (64-row passes)
+  return (size_t)(kErrorInts + tc_passes(rows, false) * (w->N / 128)) * sizeof(int);
+}
+
+size_t level_bytes_needed(int rows) {
+  // a tensor-core call parks chunk-tree levels in global scratch only when its
+  // TMEM regions are wider than 80 columns (more than 80 rows per pass)
+  if (rows <= 80) return 0;
+  return (size_t)sm_count() * kTcSpillLevels * kTcRowsMax * 128 * sizeof(float);
 }
 
 int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
@@ -603,7 +627,8 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     ra.xf[i] = sc.xf[i];
   }
   ra.layout = f.rows() ? 0 : 1;
-  ra.rp_tc = tc_rows_per_pass(rows);  // 128 for every call the clustered kernel serves
+  const bool spill = sc.lev != nullptr;
+  ra.rp_tc = tc_rows_per_pass(rows, spill);  // 128 for every call the clustered kernel serves
   const long long items = (long long)ra.rows_pad * (K / 128);
   int rc = 0;
 
@@ -613,7 +638,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   la.K = K;
   la.TK = K / 16;
   la.rows = rows;
-  const int per_pass = f.kind == kTensor ? tc_rows_per_pass(rows) : kRowsPerPass;
+  const int per_pass = f.kind == kTensor ? tc_rows_per_pass(rows, spill) : kRowsPerPass;
   la.passes = (rows + per_pass - 1) / per_pass;
   la.rp = rows < per_pass ? rows : per_pass;
   la.act = ws[0]->act;
@@ -624,7 +649,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   if (f.kind == kTensor) {
     long long blocks = 0;
     for (int i = 0; i < count; i++) blocks += ws[i]->N / 128;
-    tcG = tc_group(blocks, rows, chunks_of(K), K / 16, sm_count());
+    tcG = tc_group(blocks, rows, chunks_of(K), K / 16, sm_count(), spill);
   }
   for (int i = 0; i < count; i++) {
     const tfx_exl3_weight* w = ws[i];
@@ -671,6 +696,13 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   la.items = ctas;
   if (ctas > 0x7fffffffLL) return fail(TFX_EUNSUPPORTED, "grid of %lld CTAs", ctas);
   size_t smem = f.kind == kTensor ? kTcDynSmem : 0;
+  if (f.kind == kTensor) {
+    // the members' trellis words as 2-D tensors, boxes of 4 tiles x 4 tile rows
+    for (int i = 0; i < count; i++) {
+      rc = encode_trellis_map(ws[i], tfx::tc_word_box_words(bits), tfx::kTcBoxRows, &la.tm[i]);
+      if (rc) return rc;
+    }
+  }
   if (f.kind == kRowsWarp) {
     // tensor maps of the members' trellis words and the box shape
     long long clusters = 0;
@@ -707,7 +739,11 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ta.units = (int)ctas;
   ta.RP = per_pass;
   ta.NMf = per_pass < ra.rows_pad ? per_pass : ra.rows_pad;
+  ta.tlev = tc_tmem_levels(ta.NMf);
   ta.err = sc.err;
+  ta.lev = sc.lev;
+  if (f.kind == kTensor && __builtin_ctz(tcG) > ta.tlev && !sc.lev)
+    return fail(TFX_EUNSUPPORTED, "tensor-core launch needs chunk-tree level scratch");
   if (f.kind == kTensor) {
     const long long S = sm_count();
     ctas = ctas < S ? ctas : S;  // persistent: one CTA per SM at most
@@ -768,6 +804,41 @@ int tfx_exl3_group_into(tfx_exl3_weight* const ws[], int count, const void* x, i
   return run(ws, count, x, rows, ys, ldy, col0, stream);
 }
 
+int tfx_exl3_chain(const tfx_exl3_step* steps, int nsteps, int rows, int pdl, cudaStream_t stream) {
+  if (!steps || nsteps < 1) return fail(TFX_EINVAL, "chain of %d steps", nsteps);
+  // every step is validated (shapes, alignment, reserve) before anything is enqueued
+  for (int i = 0; i < nsteps; i++) {
+    const tfx_exl3_step& st = steps[i];
+    if (!st.ws) return fail(TFX_EINVAL, "step %d: null member list", i);
+    int rc = validate_call(st.ws, st.count, st.x, rows, st.ys, nullptr, nullptr);
+    if (rc) return fail(rc, "step %d: %s", i, g_err.c_str());
+    for (int m = 0; m < st.count; m++) {
+      const Priv* pv = static_cast<const Priv*>(st.ws[m]->priv);
+      if (!pv || pv->max_rows < rows)
+        return fail(TFX_ENOTRESERVED, "step %d member %d reserved for %d rows, chain of %d", i, m,
+                    pv ? pv->max_rows : 0, rows);
+    }
+  }
+  if (rows == 0) return 0;
+  for (int i = 0; i < nsteps; i++) {
+    const tfx_exl3_step& st = steps[i];
+    tfx::Scratch sc = {};
+    for (int m = 0; m < st.count; m++) {
+      Priv* pv = static_cast<Priv*>(st.ws[m]->priv);
+      sc.xf[m] = pv->xf;
+      sc.partial[m] = pv->partial;
+      sc.counters[m] = pv->counters + tfx::kErrorInts;
+      if (m == 0) {
+        sc.err = pv->counters;
+        sc.lev = pv->lev;
+      }
+    }
+    const int rc = tfx::launch_layer(st.ws, st.count, st.x, rows, st.ys, nullptr, nullptr, stream, sc, pdl != 0);
+    if (rc) return fail(rc, "step %d: %s", i, g_err.c_str());
+  }
+  return 0;
+}
+
 int tfx_exl3_columns(const tfx_exl3_weight* w, int from, int n, tfx_exl3_weight* view_out) {
   int rc = validate(w);
   if (rc) return rc;
@@ -800,6 +871,8 @@ int tfx_exl3_reserve(tfx_exl3_weight* w, int max_rows, cudaStream_t stream) {
   if (!rc)
     rc = grow(reinterpret_cast<void**>(&pv->counters), &pv->counter_bytes, tfx::counter_bytes_needed(w, max_rows),
               stream, pv, true);
+  if (!rc && tfx::level_bytes_needed(max_rows))
+    rc = grow(reinterpret_cast<void**>(&pv->lev), &pv->lev_bytes, tfx::level_bytes_needed(max_rows), stream, pv, false);
   if (rc) return rc;
   pv->max_rows = max_rows;
   return 0;
@@ -814,6 +887,7 @@ int tfx_exl3_release(tfx_exl3_weight* w) {
   if (pv->xf) d.free(pv->xf, nullptr);
   if (pv->partial) d.free(pv->partial, nullptr);
   if (pv->counters) d.free(pv->counters, nullptr);
+  if (pv->lev) d.free(pv->lev, nullptr);
   if (d.alloc == rt_alloc) cudaDeviceSynchronize();
   delete pv;
   w->priv = nullptr;
@@ -851,8 +925,9 @@ int tfx_exl3_debug_launch_shape(int K, int bits, int rows, int64_t blocks, int s
                             "blocks >= 1, sm_count >= 0, non-null outputs");
   const Family f = pick(bits, rows);
   *family = (int)f.kind;
-  *chunks_per_unit =
-      f.kind == kTensor ? tc_group(blocks, rows, tfx::chunks_of(K), K / 16, sm_count_ ? sm_count_ : sm_count()) : 0;
+  *chunks_per_unit = f.kind == kTensor ? tc_group(blocks, rows, tfx::chunks_of(K), K / 16,
+                                                  sm_count_ ? sm_count_ : sm_count(), true)
+                                         : 0;
   return 0;
 }
 

@@ -14,7 +14,8 @@ struct Scratch {
   uint2* xf[3];
   float* partial[3];
   int* counters[3];
-  int* err;  // device error word (a bounded wait gave up)
+  int* err;    // device error word (a bounded wait gave up)
+  float* lev;  // tensor-core chunk-tree level slots (null: passes of at most 64 rows above 128 rows)
 };
 
 // The counter buffer of a weight starts with this many ints: word 0 is the
@@ -27,6 +28,7 @@ int chunks_of(int K);
 size_t xf_bytes_needed(const tfx_exl3_weight* w, int rows);
 size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows);
 size_t counter_bytes_needed(const tfx_exl3_weight* w, int rows);
+size_t level_bytes_needed(int rows);
 // Enqueue the rotation and the linear launch for validated members on `s`;
 // ldy / col0 give each member's output window (null: N and 0).
 int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],

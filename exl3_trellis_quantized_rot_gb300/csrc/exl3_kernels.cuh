@@ -858,8 +858,9 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
     }
   }
   __syncthreads();
-  // no early trigger here: the next call's kernels launch when this one ends
-  // (an early trigger lets them occupy SM resources for the whole kernel)
+  // the dependent launch is triggered after the chain loop, not here: an
+  // early trigger lets the next kernel's CTAs occupy SM resources for the
+  // whole kernel
   griddep_wait();
   // x stage of box b: the chunk's tiles [b*H, min(n, (b+1)*H)) of every row
   // group q (or, with a whole-chunk stage, all n tiles at once), each one
@@ -981,6 +982,11 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
     }
   }
   if (!alive && lane == 0) s_dead = 1;
+  // with programmatic dependent launch, the next kernel may start launching
+  // once every CTA is past its chain loop: all of this kernel's CTAs are then
+  // resident, so the dependents' CTAs (which wait for this grid before they
+  // read its output) only overlap the cluster epilogue
+  griddep_launch();
   __syncthreads();
   const bool dead = s_dead != 0;
   if (dead) {

@@ -16,74 +16,97 @@
 // The kernel is persistent: one CTA per SM walks the work units
 // (member, pass, 128-column block, chunk group) in a fixed stride. The work
 // of a unit is cut into stages of kTcSK k-steps that flow through warp roles:
-//   warps 0..15   decode: load their tiles' words straight from global memory
-//                 into a ring of register slots (up to two stages ahead) and
-//                 turn 4 tiles per stage into FP16 A operands;
-//   warps 16..19  fold: merge each finished chunk into the chunk tree (levels
-//                 parked in TMEM), then write the unit's output: the whole
-//                 rot_out epilogue when one unit covers all C chunks, else its
-//                 FP32 slab, which tc_combine_kernel folds afterwards;
+//   warp 22       asks the tensor copy engine for each stage's trellis words
+//                 (2-D boxes of 4 tile rows x 4 tiles) into a ring of
+//                 tc_word_stages(BITS) stages, as far ahead as the ring allows;
+//   warp 21       bulk-copies the x rows of each stage (lanes 0..3, a slice each);
+//   warps 0..15   decode: turn 4 tiles of each stage into FP16 A operands;
 //   warp 20       issues the MMAs strictly in k order (lane 0);
-//   warp 21       bulk-copies the x rows of each stage (lanes 0..3, a slice each).
-// The decode warps hand a filled A buffer to the MMA warp, and the fold warps
-// hand a folded TMEM region back to it, through hardware named barriers
-// (waiting warps are descheduled, nothing polls). Completions of the
-// asynchronous units (bulk copies, MMAs) are mbarriers that lane 0 of each
-// waiting warp polls; the decode warps and the x warp wait on the MMA
-// completion of the buffer they refill themselves, so that the MMA warp's
-// loop is only ready barrier, x wait, MMA issue and commit. A waiter cannot
-// fall two phases behind on such a barrier: its next completion needs the
-// waiter's own next stage first. Every mbarrier wait is bounded: on a
-// timeout the kernel records an error and from then on skips all work while
-// still taking every named barrier, so each warp reaches the end and TMEM is
-// released.
+//   warps 16..19  fold: merge each finished chunk into the chunk tree, then
+//                 write the unit's output: the whole rot_out epilogue when one
+//                 unit covers all C chunks; otherwise the unit's FP32 subtree
+//                 sum goes to its slab, and tc_combine_kernel folds a block's
+//                 slabs afterwards, one warp per (row, block), all in parallel.
+//                 (The pages' form, where the unit that arrives last on the
+//                 block's counter folds the slabs, was built here and measured
+//                 on GB300 at 3-5x the time of a call: one CTA's four fold
+//                 warps then read P x rows x 512 B of slabs from L2 one round
+//                 trip per 4 rows while that CTA's own pipeline waits.)
+// Every hand-off is an mbarrier: full/empty rings for words (copy engine ->
+// decode warps -> word warp), x (copy engine -> MMA warp; MMA completion ->
+// x warp), A buffers (decode warps -> MMA warp; MMA completion -> decode
+// warps) and the two TMEM accumulator regions (MMA completion -> fold warps;
+// fold warps -> MMA warp). A waiter never falls two phases behind: the next
+// completion of any of these barriers needs the waiter's own next step first.
+// Every wait is bounded by the launch's spin limit. On a timeout the kernel
+// records device error 1 and every role leaves its loop at its next wait (the
+// waits see the abort flag); before the CTA ends, every thread waits about a
+// millisecond so that copies and MMAs in flight land, then TMEM is freed.
+//
+// The chunk tree parks one partial sum per level (up to log2(16) = 4). TMEM
+// holds two accumulator regions plus the first `tlev` levels of NMf columns
+// each within its 512 columns; deeper levels go to a per-CTA slot of global
+// scratch (L2-resident, written and read back by the same thread). That lets
+// one unit hold all C chunks of a 128-row pass, so each weight is decoded once
+// per 128 rows.
 #pragma once
 #include "exl3_kernels.cuh"
 
 namespace tfx {
 
-constexpr int kTcRowsMax = 128;   // rows per pass (MMA N) when a call has at most this many rows
-constexpr int kTcRowsLong = 64;   // rows per pass above that (keeps all C chunks in one CTA)
-constexpr int kTcSK = 8;          // k-steps per stage
+constexpr int kTcRowsMax = 128;      // rows per pass (MMA N)
+constexpr int kTcRowsNoSpill = 64;   // rows per pass above 128 rows when no level scratch is given
+constexpr int kTcSK = 8;             // k-steps per stage
 constexpr int kTcDecodeWarps = 16;
-constexpr int kTcFoldWarp0 = 16;  // 4 fold warps; TMEM lane quarter = warp % 4
+constexpr int kTcFoldWarp0 = 16;     // 4 fold warps; TMEM lane quarter = warp % 4
 constexpr int kTcMmaWarp = 20;
 constexpr int kTcXWarp = 21;
-constexpr int kTcThreads = 22 * 32;
+constexpr int kTcWWarp = 22;
+constexpr int kTcThreads = 23 * 32;
 constexpr int kTcXS = 3;                              // x ring stages
 constexpr int kTcXLanes = 4;                          // lanes that copy a stage's x (one slice each)
 constexpr int kTcXStage = kTcSK * kTcRowsMax * 32;    // x bytes per stage (32 KB)
-constexpr int kTcAB = 3;                              // A (decoded weight) buffers
+constexpr int kTcAB = 2;                              // A (decoded weight) buffers
 constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (32 KB)
+constexpr int kTcWRing = 48 * 1024;                   // trellis-word ring
+constexpr int kTcBoxRows = 4;                         // tile rows per word box
 constexpr int kTcExBytes = 2 * 4 * 128 * 4;           // epilogue exchange (two 4-row groups)
-constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcExBytes;
-// named barriers (0 is __syncthreads)
-constexpr int kBarFold = 1;        // the 4 fold warps
-constexpr int kBarReady = 2;       // + A buffer: decode warps -> MMA warp (3 ids)
-constexpr int kBarFolded = 5;      // + chunk parity: fold warps -> MMA warp (2 ids)
-constexpr int kReadyThreads = (kTcDecodeWarps + 1) * 32;
-constexpr int kFoldedThreads = 5 * 32;
+constexpr int kTcMaxLevels = 4;                       // chunk tree levels (C <= 16)
+constexpr int kTcSpillLevels = 2;                     // levels a CTA may park in global scratch
+constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcWRing + kTcExBytes;
+constexpr int kBarFold = 1;  // named barrier of the 4 fold warps (0 is __syncthreads)
 
-// Wait for the phase of the given parity to complete, at most `spin` cycles.
-// The thread polls with the non-blocking test (a try_wait on an incomplete
-// phase suspends the thread for a fixed slice instead of until completion),
-// sleeping sleep_ns between polls so that waiting warps leave the issue slots
-// of their scheduler to the warps doing work.
+// Trellis words of one stage (kTcSK tile rows of a 128-column block) and how
+// many stages the ring holds (at most 8).
+__host__ __device__ constexpr int tc_word_stage_bytes(int bits) { return kTcSK * 64 * bits * 4; }
+__host__ __device__ constexpr int tc_word_stages(int bits) {
+  return kTcWRing / tc_word_stage_bytes(bits) > 8 ? 8 : kTcWRing / tc_word_stage_bytes(bits);
+}
+// One word box: kTcBoxRows tile rows x 4 tiles (half a block), 32*bits words per row.
+__host__ __device__ constexpr int tc_word_box_words(int bits) { return 32 * bits; }
+__host__ __device__ constexpr int tc_word_box_bytes(int bits) { return kTcBoxRows * 32 * bits * 4; }
+
+// Wait for the phase of the given parity to complete, at most `spin` cycles;
+// gives up at once when the CTA has aborted. On its own timeout it aborts the
+// CTA and records device error 1. After one non-blocking test, the thread
+// waits with try_wait and a suspend-time hint: it is parked (it issues no
+// instructions) until the phase completes or the hint runs out, so waiting
+// warps leave the issue slots of their scheduler to the decode warps. (A
+// spinning test_wait loop in the MMA warp alone issued about half of the
+// kernel's instructions, measured with ncu on GB300.)
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
-                                          long long spin, int sleep_ns = 0) {
-  if (*abort_flag) return false;
+                                          long long spin) {
   if (mbar_poll(b, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_poll(b, parity)) {
+  while (true) {
     if (*abort_flag) return false;
-    if (sleep_ns) __nanosleep(sleep_ns);
     if (clock64() - t0 > spin) {
       *abort_flag = 1;
       atomicExch(err, 1);
       return false;
     }
+    if (mbar_test_sleep(b, parity, 20000u)) return true;
   }
-  return true;
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -110,30 +133,33 @@ __device__ __forceinline__ void umma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s_addr(b))
                : "memory");
 }
-// 4 consecutive TMEM columns of this warp's 32 lanes.
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
-  uint32_t r[4];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(taddr)
-               : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 4; i++) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, const float (&v)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(__float_as_uint(v[0])),
-               "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3]))
-               : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-constexpr int kTcMaxLevels = 4;  // chunk tree levels parked in TMEM (C <= 16)
 
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-__device__ __forceinline__ void bar_arrive(int id, int n) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+
+// 16 consecutive TMEM columns of this warp's 32 lanes, without waiting: the
+// registers are valid after tmem_wait_ld (several loads share one round trip).
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 16 consecutive TMEM columns stored without waiting (tmem_wait_st before the
+// columns are read again or handed to another thread).
+__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive TMEM columns of this warp's 32 lanes (one round trip).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -174,11 +200,14 @@ __host__ __device__ __forceinline__ long long xc_byte(int r, int k, int K, int R
 }
 
 struct TcArgs {
-  LinearArgs la;   // la.m[i].cta_begin is the member's first unit; la.rp the slab row stride
-  int units;       // work units of all members
-  int RP;          // rows per pass
-  int NMf;         // TMEM columns per region: min(RP, rows_pad)
-  int* err;        // device error word: 1 when a wait timed out, 2 on a short shared-memory launch
+  LinearArgs la;  // la.m[i].cta_begin is the member's first unit; la.rp the slab row stride;
+                  // la.tm[i] member i's trellis words, boxes of 4 tiles x kTcBoxRows tile rows
+  int units;      // work units of all members
+  int RP;         // rows per pass
+  int NMf;        // TMEM columns per region: min(RP, rows_pad)
+  int tlev;       // chunk tree levels parked in TMEM; deeper ones go to `lev`
+  int* err;       // device error word: 1 when a wait timed out, 2 on a short shared-memory launch
+  float* lev;     // global scratch for deeper levels: per CTA, kTcSpillLevels x NMf x 128 FP32
 };
 
 struct TcUnit {
@@ -195,8 +224,8 @@ __device__ __forceinline__ TcUnit tc_unit(const TcArgs& ta, int u) {
   if (a.count > 2 && u >= a.m[2].cta_begin) U.mi = 2;
   const Member& M = a.m[U.mi];
   int local = u - M.cta_begin;
-  U.gidx = local % M.P;
-  local /= M.P;
+  U.gidx = local & (M.P - 1);  // P is a power of two
+  local >>= ilog2_pow2(M.P);
   U.nb = local % M.NB;
   U.pass = local / M.NB;
   const int c0 = U.gidx * M.G;
@@ -221,9 +250,9 @@ __device__ __forceinline__ bool fold_all(bool ok) {
 }
 // One lane polls, the warp follows with a warp-uniform outcome.
 __device__ __forceinline__ bool wait_lane0(uint64_t* b, uint32_t parity, volatile int* abort_flag, int* err,
-                                           long long spin, int lane, int sleep_ns) {
+                                           long long spin, int lane) {
   int ok = 1;
-  if (lane == 0) ok = mbar_wait(b, parity, abort_flag, err, spin, sleep_ns);
+  if (lane == 0) ok = mbar_wait(b, parity, abort_flag, err, spin);
   ok = __shfl_sync(0xffffffffu, ok, 0);
   return ok != 0;
 }
@@ -231,7 +260,8 @@ __device__ __forceinline__ bool wait_lane0(uint64_t* b, uint32_t parity, volatil
 // Rows r0..r0+3 of one 128-column block, thread = column n = 32*(warp%4) + lane
 // of the four fold warps: finish the Walsh-Hadamard transform over n in the
 // same stage order as fwht128 (n bits 0..4 across lanes, then bits 5 and 6
-// through shared memory), scale by 1/sqrt(128) and svh, store y.
+// through shared memory), scale by 1/sqrt(128) and svh, store y (rows below
+// nrows only).
 __device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane, float* ex, float sv, const Member& M,
                                                  long long row0, int ncol, int nrows, int act) {
 #pragma unroll
@@ -260,20 +290,22 @@ __device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane,
 
 template <int BITS>
 __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_constant__ TcArgs ta) {
-  using WF = WordFetch<BITS>;
   constexpr int kH = kTcSK / 2;  // tiles per decode warp per stage
+  constexpr int WS = tc_word_stages(BITS);
+  constexpr int WSB = tc_word_stage_bytes(BITS);
+  constexpr int BOXB = tc_word_box_bytes(BITS);
   const LinearArgs& a = ta.la;
   extern __shared__ __align__(1024) unsigned char dsm[];
-  unsigned char* sX = dsm;                                  // [kTcXS][kTcXStage]
-  unsigned char* sA = sX + kTcXS * kTcXStage;               // [kTcAB][kTcAStage]
-  float* sEx = reinterpret_cast<float*>(sA + kTcAB * kTcAStage);  // [2][4][128]
-  static_assert(kTcAB == kTcXS, "one commit per stage frees its A buffer and its x slot");
-  __shared__ __align__(8) uint64_t xfull[kTcXS], sdone[kTcAB], chunk_done[2];
+  unsigned char* sX = dsm;                               // [kTcXS][kTcXStage]
+  unsigned char* sA = sX + kTcXS * kTcXStage;            // [kTcAB][kTcAStage]
+  unsigned char* sW = sA + kTcAB * kTcAStage;            // [WS][WSB]
+  float* sEx = reinterpret_cast<float*>(sW + kTcWRing);  // [2][4][128]
+  __shared__ __align__(8) uint64_t xfull[kTcXS], xdone[kTcXS], afull[kTcAB], adone[kTcAB], wfull[8], wempty[8],
+      cdone[2], tfree[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
   griddep_wait();
-  griddep_launch();
   {
     // the launch must provide the shared memory the kernel lays out
     uint32_t dyn;
@@ -284,19 +316,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     }
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // TMEM: two accumulator regions plus log2(G) parked tree levels of NMf columns
+  const long long spin = a.spin;
+  // TMEM: two accumulator regions plus the parked tree levels kept in TMEM
   int maxlog = a.m[0].log2G;
   for (int i = 1; i < a.count; i++) maxlog = max(maxlog, a.m[i].log2G);
   uint32_t tmem_cols = 32;
-  while (tmem_cols < (uint32_t)((2 + maxlog) * ta.NMf)) tmem_cols *= 2;
+  while (tmem_cols < (uint32_t)((2 + min(maxlog, ta.tlev)) * ta.NMf)) tmem_cols *= 2;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int i = 0; i < kTcXS; i++) {
       mbar_init(&xfull[i], 1);
+      mbar_init(&xdone[i], 1);
     }
-    for (int i = 0; i < kTcAB; i++) mbar_init(&sdone[i], 1);
-    for (int i = 0; i < 2; i++) mbar_init(&chunk_done[i], 1);
+    for (int i = 0; i < kTcAB; i++) {
+      mbar_init(&afull[i], kTcDecodeWarps);
+      mbar_init(&adone[i], 1);
+    }
+    for (int i = 0; i < WS; i++) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], kTcDecodeWarps);
+    }
+    for (int i = 0; i < 2; i++) {
+      mbar_init(&cdone[i], 1);
+      mbar_init(&tfree[i], 4);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kTcMmaWarp) {
@@ -318,78 +362,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     lw.init(lane);
     const int g = lane >> 2, t = lane & 3;
     const int off0 = 512 * j + 16 * g + 4 * t;  // A-fragment register 0 in the core-matrix layout
-    // the words of stage gs sit in register slot gs % NS; the slot of the
-    // stage just decoded is refilled with the words NS-1 stages ahead, so a
-    // load has NS-1 stages of decode to land (the loop is unrolled NS times
-    // so that every slot is a fixed set of registers: no in-flight load is
-    // ever copied)
-    constexpr int NS = WF::kOwn <= 2 ? 3 : 2;
-    uint32_t own[NS][kH][WF::kOwn];
-    auto load_stage = [&](const TcUnit& U, int s0, uint32_t (&dst)[kH][WF::kOwn]) {
-      const Member& M = a.m[U.mi];
-      const uint32_t* col = M.trellis + (long long)(U.nb * 8 + j) * (8 * BITS);
+    // tile (q0 + h, j) of a word stage: box (q0/4, j/4), row h, tile j%4
+    const int wofs = ((q0 / kTcBoxRows) * 2 + (j >> 2)) * BOXB + (j & 3) * 32 * BITS;
+    int gs = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
+      const TcUnit U = tc_unit(ta, u);
+      for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
+        const int cnt = min(kTcSK, U.nsteps - s0);
+        const int ws = gs % WS, ab = gs % kTcAB;
+        ok = wait_lane0(&wfull[ws], (uint32_t)(gs / WS) & 1u, &s_abort, ta.err, spin, lane);
+        // buffer ab last held stage gs - kTcAB: its MMAs must have completed
+        if (ok && gs >= kTcAB)
+          ok = wait_lane0(&adone[ab], (uint32_t)((gs - kTcAB) / kTcAB) & 1u, &s_abort, ta.err, spin, lane);
+        if (!ok) break;
+        const unsigned char* wst = sW + ws * WSB + wofs;
+        unsigned char* abuf = sA + ab * kTcAStage;
 #pragma unroll
-      for (int h = 0; h < kH; h++)
-        if (s0 + q0 + h < U.nsteps) WF::load(col + (long long)(U.tbeg + s0 + q0 + h) * M.stride, lw, lane, dst[h]);
-    };
-    // stage iterators: (u, s0, U) the stage to decode, (lu, ls0, LU) the next one to load
-    int u = blockIdx.x, s0 = 0, gs = 0;
-    TcUnit U;
-    if (u < ta.units) U = tc_unit(ta, u);
-    int lu = u, ls0 = 0;
-    TcUnit LU = U;
-    auto advance = [&](int& uu, int& ss, TcUnit& UU) {
-      ss += kTcSK;
-      if (ss >= UU.nsteps) {
-        uu += gridDim.x;
-        ss = 0;
-        if (uu < ta.units) UU = tc_unit(ta, uu);
-      }
-    };
-#pragma unroll
-    for (int sl = 0; sl < NS - 1; sl++) {
-      if (lu < ta.units) {
-        load_stage(LU, ls0, own[sl]);
-        advance(lu, ls0, LU);
-      }
-    }
-    while (u < ta.units) {
-#pragma unroll
-      for (int sl = 0; sl < NS; sl++) {
-        if (u < ta.units) {
-          // refill the slot decoded last (stage gs-1) with stage gs+NS-1
-          if (lu < ta.units) {
-            load_stage(LU, ls0, own[(sl + NS - 1) % NS]);
-            advance(lu, ls0, LU);
+        for (int h = 0; h < kH; h++) {
+          if (q0 + h < cnt) {
+            const uint32_t* tile = reinterpret_cast<const uint32_t*>(wst + h * 128 * BITS);
+            uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
+            raw[0] = tile[lw.i0];
+            raw[1] = tile[lw.i1];
+            if constexpr (Geo<BITS>::kRaw > 2) raw[2] = tile[lw.i2];
+            lw.align(raw, win);
+            decode8<BITS>(win, af);
+            unsigned char* o = abuf + (q0 + h) * 4096 + off0;
+            *reinterpret_cast<uint32_t*>(o) = af[0];        // n = g,   k = 2t..
+            *reinterpret_cast<uint32_t*>(o + 256) = af[1];  // n = g+8, k = 2t..
+            *reinterpret_cast<uint32_t*>(o + 128) = af[2];  // n = g,   k = 2t+8..
+            *reinterpret_cast<uint32_t*>(o + 384) = af[3];  // n = g+8, k = 2t+8..
           }
-          const int cnt = min(kTcSK, U.nsteps - s0);
-          const int ab = gs % kTcAB;
-          // buffer ab last held stage gs - kTcAB: wait until its MMAs completed
-          if (gs >= kTcAB) {
-            if (lane == 0) mbar_wait(&sdone[ab], ((gs - kTcAB) / kTcAB) & 1, &s_abort, ta.err, a.spin);
-            __syncwarp();
-          }
-          if (!s_abort) {
-            unsigned char* abuf = sA + ab * kTcAStage;
-#pragma unroll
-            for (int h = 0; h < kH; h++) {
-              if (q0 + h < cnt) {
-                uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
-                WF::gather(own[sl][h], lw, lane, raw);
-                lw.align(raw, win);
-                decode8<BITS>(win, af);
-                unsigned char* o = abuf + (q0 + h) * 4096 + off0;
-                *reinterpret_cast<uint32_t*>(o) = af[0];        // n = g,   k = 2t..
-                *reinterpret_cast<uint32_t*>(o + 256) = af[1];  // n = g+8, k = 2t..
-                *reinterpret_cast<uint32_t*>(o + 128) = af[2];  // n = g,   k = 2t+8..
-                *reinterpret_cast<uint32_t*>(o + 384) = af[3];  // n = g+8, k = 2t+8..
-              }
-            }
-            fence_async_smem();
-          }
-          bar_arrive(kBarReady + ab, kReadyThreads);
-          gs++;
-          advance(u, s0, U);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&afull[ab]);
+          mbar_arrive(&wempty[ws]);
         }
       }
     }
@@ -397,115 +407,158 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     // ---------------- fold and output: thread = TMEM lane = column n of the block
     const int lg = warp & 3, n = 32 * lg + lane;
     const uint32_t lane_base = (uint32_t)(lg * 32) << 16;
+    float* spill = ta.lev ? ta.lev + (size_t)blockIdx.x * kTcSpillLevels * NMf * 128 + n : nullptr;
     int gc = -1, exb = 0;
-    for (int u = blockIdx.x; u < ta.units; u += gridDim.x) {
+    bool ok = true;
+    for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
       const TcUnit U = tc_unit(ta, u);
       const Member& M = a.m[U.mi];
       const float sv = __half2float(M.svh[U.nb * 128 + n]);
       const long long slab = (long long)a.rp * M.N;
       for (int c = 0; c < M.G; c++) {
         gc++;
-        const bool ok = fold_all(wait_lane0(&chunk_done[gc & 1], (gc >> 1) & 1, &s_abort, ta.err, a.spin, lane, 64));
-        if (ok) {
-          tc_fence_after();
-          const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * NMf);
-          const bool final = c + 1 == M.G;
-          // 16 columns (rows of the pass) at a time: cur + the levels the tree
-          // prescribes, parked again or written out
-          for (int cc = 0; cc < U.NMp; cc += 16) {
-            float v[16];
-            tmem_ld16(cur + (uint32_t)cc, v);
-            int l = 0;
-            for (; l < kTcMaxLevels && ((c >> l) & 1); l++) {
-              float w[16];
-              tmem_ld16(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), w);
+        ok = fold_all(wait_lane0(&cdone[gc & 1], (uint32_t)(gc >> 1) & 1u, &s_abort, ta.err, spin, lane));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * NMf);
+        const bool final = c + 1 == M.G;
+        // the levels this chunk closes: c's trailing one bits (all of them for
+        // the unit's last chunk), the first `tlev` of them in TMEM
+        int nlev = 0;
+        while (nlev < kTcMaxLevels && ((c >> nlev) & 1)) nlev++;
+        const int nt = min(nlev, ta.tlev);
+        // 16 columns (rows of the pass) at a time: cur + the levels the tree
+        // prescribes (level 0 first), parked again or written out. The TMEM
+        // loads of a group share one round trip; stores are not waited for
+        // until the chunk is done.
+        for (int cc = 0; cc < U.NMp; cc += 16) {
+          float v[16];
+          {
+            uint32_t r0[16], r1[16], r2[16];
+            tmem_ld16_async(cur + (uint32_t)cc, r0);
+            if (nt > 0) tmem_ld16_async(tmem + lane_base + (uint32_t)(2 * NMf + cc), r1);
+            if (nt > 1) tmem_ld16_async(tmem + lane_base + (uint32_t)(3 * NMf + cc), r2);
+            tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 16; e++) v[e] = w[e] + v[e];
+            for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r0[e]);
+            if (nt > 0)
+#pragma unroll
+              for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r1[e]) + v[e];
+            if (nt > 1)
+#pragma unroll
+              for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r2[e]) + v[e];
+            if (nt > 2) {
+              tmem_ld16_async(tmem + lane_base + (uint32_t)(4 * NMf + cc), r1);
+              if (nt > 3) tmem_ld16_async(tmem + lane_base + (uint32_t)(5 * NMf + cc), r2);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r1[e]) + v[e];
+              if (nt > 3)
+#pragma unroll
+                for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r2[e]) + v[e];
             }
-            if (!final) {
-              tmem_st16(tmem + lane_base + (uint32_t)((2 + l) * NMf + cc), v);
-            } else if (M.P == 1) {
+            // levels parked in global scratch (only chunks that close a level
+            // beyond TMEM's: two of every 16 when two levels are parked there)
+            if (nlev > ta.tlev) {
+              const float* src0 = spill + (size_t)cc * 128;
 #pragma unroll
-              for (int q = 0; q < 4; q++) {
-                float v4[4] = {v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]};
-                tc_rot_out_store(v4, n, lane, sEx + (exb & 1) * 512, sv, M, U.row0 + cc + 4 * q, U.nb * 128 + n,
-                                 U.prow - cc - 4 * q, a.act);
-                exb++;
+              for (int e = 0; e < 16; e++) v[e] = __ldcg(src0 + e * 128) + v[e];
+              if (nlev > ta.tlev + 1) {
+                const float* src = spill + (size_t)(NMf + cc) * 128;
+#pragma unroll
+                for (int e = 0; e < 16; e++) v[e] = __ldcg(src + e * 128) + v[e];
               }
-            } else {
-              float* part =
-                  M.partial + ((long long)U.pass * M.P + U.gidx) * slab + (long long)cc * M.N + U.nb * 128 + n;
-#pragma unroll
-              for (int e = 0; e < 16; e++)
-                if (cc + e < U.prow) part[(long long)e * M.N] = v[e];
             }
           }
-          tc_fence_before();
+          if (!final) {
+            // park at level nlev (the first clear bit of c)
+            if (nlev < ta.tlev) {
+              tmem_st16_async(tmem + lane_base + (uint32_t)((2 + nlev) * NMf + cc), v);
+            } else {
+              float* dst = spill + (size_t)((nlev - ta.tlev) * NMf + cc) * 128;
+#pragma unroll
+              for (int e = 0; e < 16; e++) __stcg(dst + e * 128, v[e]);
+            }
+          } else if (M.P == 1) {
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+              float v4[4] = {v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]};
+              tc_rot_out_store(v4, n, lane, sEx + (exb & 1) * 512, sv, M, U.row0 + cc + 4 * q, U.nb * 128 + n,
+                               U.prow - cc - 4 * q, a.act);
+              exb++;
+            }
+          } else {
+            float* part = M.partial + ((long long)U.pass * M.P + U.gidx) * slab + (long long)cc * M.N + U.nb * 128 + n;
+#pragma unroll
+            for (int e = 0; e < 16; e++)
+              if (cc + e < U.prow) __stcg(part + (long long)e * M.N, v[e]);
+          }
         }
-        bar_arrive(kBarFolded + (gc & 1), kFoldedThreads);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfree[gc & 1]);
       }
     }
   } else if (warp == kTcMmaWarp) {
-    // ---------------- MMA issue, strictly in k order; lane 0 issues, the warp takes the barriers
-    const uint64_t da0 = umma_desc(sA), db0 = umma_desc(sX);
-    int gs = 0, gc = -1;
-    for (int u = blockIdx.x; u < ta.units; u += gridDim.x) {
-      const TcUnit U = tc_unit(ta, u);
-      const Member& M = a.m[U.mi];
-      const uint32_t idesc = umma_idesc(U.NMp);
-      const int log2C = __ffs(M.C) - 1;
-      const int c0 = U.gidx * M.G;
-      int ci = -1, cnext = 0;
-      uint32_t acc = 0, dcol = 0;
-      for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
-        const int cnt = min(kTcSK, U.nsteps - s0);
-        const int ab = gs % kTcAB, xs = gs % kTcXS;
-        bar_sync(kBarReady + ab, kReadyThreads);
-        int okx = 1;
-        if (lane == 0) okx = mbar_wait(&xfull[xs], (gs / kTcXS) & 1, &s_abort, ta.err, a.spin);
-        okx = __shfl_sync(0xffffffffu, okx, 0);
-        tc_fence_after();
-        const bool go = okx && !s_abort;
-        const uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
-        const uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
-        const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
-        // the stage's k-steps as runs inside one chunk: a chunk start first
-        // resets the accumulator (and waits until its TMEM region was folded),
-        // then lane 0 issues the run back to back and, if the run ends the
-        // chunk, commits it to the fold warps
-        for (int q = 0; q < cnt;) {
-          if (s0 + q == cnext) {
-            ci++;
-            gc++;
-            acc = 0;
-            dcol = (uint32_t)((gc & 1) * NMf);
-            cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
-            // the region of chunk gc last held chunk gc-2: it must have been folded
-            if (gc >= 2) bar_sync(kBarFolded + (gc & 1), kFoldedThreads);
-            tc_fence_after();
-          }
-          const int qe = min(cnt, cnext - s0);
-          if (lane == 0) {
-            if (go)
-              for (int i = q; i < qe; i++) {
-                umma_f16(tmem + dcol, da + (uint64_t)(i * (4096 >> 4)), db + (uint64_t)(i * db_step), idesc, acc);
-                acc = 1;
+    // ---------------- MMA issue, strictly in k order, by lane 0
+    if (lane == 0) {
+      const uint64_t da0 = umma_desc(sA), db0 = umma_desc(sX);
+      int gs = 0, gc = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
+        const TcUnit U = tc_unit(ta, u);
+        const Member& M = a.m[U.mi];
+        const uint32_t idesc = umma_idesc(U.NMp);
+        const int log2C = ilog2_pow2(M.C);
+        const int c0 = U.gidx * M.G;
+        int ci = -1, cnext = 0;
+        uint32_t acc = 0, dcol = 0;
+        for (int s0 = 0; s0 < U.nsteps && ok; s0 += kTcSK, gs++) {
+          const int cnt = min(kTcSK, U.nsteps - s0);
+          const int ab = gs % kTcAB, xs = gs % kTcXS;
+          ok = mbar_wait(&afull[ab], (uint32_t)(gs / kTcAB) & 1u, &s_abort, ta.err, spin) &&
+               mbar_wait(&xfull[xs], (uint32_t)(gs / kTcXS) & 1u, &s_abort, ta.err, spin);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
+          const uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
+          const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
+          // the stage's k-steps as runs inside one chunk: a chunk start first
+          // resets the accumulator (and waits until its TMEM region was
+          // folded), then the run issues back to back and, if it ends the
+          // chunk, commits it to the fold warps
+          for (int q = 0; q < cnt;) {
+            if (s0 + q == cnext) {
+              ci++;
+              gc++;
+              acc = 0;
+              dcol = (uint32_t)((gc & 1) * NMf);
+              cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
+              // the region of chunk gc last held chunk gc-2: it must have been folded
+              if (gc >= 2) {
+                ok = mbar_wait(&tfree[gc & 1], (uint32_t)((gc - 2) >> 1) & 1u, &s_abort, ta.err, spin);
+                if (!ok) break;
               }
-            if (s0 + qe == cnext) umma_commit(&chunk_done[gc & 1]);
+              tc_fence_after();
+            }
+            const int qe = min(cnt, cnext - s0);
+            for (int i = q; i < qe; i++) {
+              umma_f16(tmem + dcol, da + (uint64_t)(i * (4096 >> 4)), db + (uint64_t)(i * db_step), idesc, acc);
+              acc = 1;
+            }
+            if (s0 + qe == cnext) umma_commit(&cdone[gc & 1]);
+            q = qe;
           }
-          acc = 1;
-          q = qe;
+          if (!ok) break;
+          // frees A buffer ab and x slot xs once these MMAs have completed
+          umma_commit(&adone[ab]);
+          umma_commit(&xdone[xs]);
         }
-        // frees A buffer ab and x slot xs (the same index): the decode warps
-        // and the x warp wait on it themselves
-        if (lane == 0) umma_commit(&sdone[ab]);
-        __syncwarp();
       }
     }
-    // the folds of the last two chunks
-    for (int c = gc - 1; c <= gc; c++)
-      if (c >= 0) bar_sync(kBarFolded + (c & 1), kFoldedThreads);
-  } else {
+    __syncwarp();
+  } else if (warp == kTcXWarp) {
     // ---------------- x rows of the pass: one contiguous run per stage, cut
     // into kTcXLanes slices that as many lanes copy: the bulk copies of one
     // thread complete one after another (measured on GB300: about one per
@@ -513,7 +566,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     if (lane < kTcXLanes) {
       constexpr unsigned kMask = (1u << kTcXLanes) - 1;
       int gs = 0;
-      for (int u = blockIdx.x; u < ta.units; u += gridDim.x) {
+      bool ok = true;
+      for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
         const TcUnit U = tc_unit(ta, u);
         const Member& M = a.m[U.mi];
         const unsigned char* xsrc =
@@ -521,10 +575,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
           const int cnt = min(kTcSK, U.nsteps - s0);
           const int xs = gs % kTcXS;
-          int ok = 1;
-          if (lane == 0 && gs >= kTcXS) ok = mbar_wait(&sdone[xs], ((gs - kTcXS) / kTcXS) & 1, &s_abort, ta.err, a.spin, 32);
-          ok = __shfl_sync(kMask, ok, 0);
-          if (!ok || s_abort) continue;
+          int okl = 1;
+          if (lane == 0 && gs >= kTcXS)
+            okl = mbar_wait(&xdone[xs], (uint32_t)((gs - kTcXS) / kTcXS) & 1u, &s_abort, ta.err, spin);
+          ok = __shfl_sync(kMask, okl, 0) != 0;
+          if (!ok) break;
           // bytes = cnt * NMp * 32 is a multiple of 512: every slice is a multiple of 16 bytes
           const uint32_t bytes = (uint32_t)(cnt * U.NMp * 32), slice = bytes / kTcXLanes;
           if (lane == 0) mbar_expect_tx(&xfull[xs], bytes);
@@ -533,14 +588,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
                    xsrc + (long long)(U.tbeg + s0) * U.NMp * 32 + (long long)lane * slice, slice, &xfull[xs]);
         }
       }
-      if (s_abort) {
-        // let copies already in flight land before the CTA's shared memory goes away
-        const long long t0 = clock64();
-        while (clock64() - t0 < 2000000) {
+    }
+    __syncwarp();
+  } else {
+    // ---------------- trellis words: per stage, 2-D boxes of 4 tiles x 4 tile
+    // rows (two per 4 rows of the stage) into the ring; a slot is refilled
+    // once all 16 decode warps have consumed it
+    if (lane == 0) {
+      int gs = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
+        const TcUnit U = tc_unit(ta, u);
+        const CUtensorMap* tm = &a.tm[U.mi];
+        for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
+          const int ws = gs % WS;
+          if (gs >= WS) {
+            ok = mbar_wait(&wempty[ws], (uint32_t)((gs - WS) / WS) & 1u, &s_abort, ta.err, spin);
+            if (!ok) break;
+          }
+          const int nrb = (min(kTcSK, U.nsteps - s0) + kTcBoxRows - 1) / kTcBoxRows;
+          mbar_expect_tx(&wfull[ws], (uint32_t)(nrb * 2 * BOXB));
+          for (int rb = 0; rb < nrb; rb++)
+            for (int hx = 0; hx < 2; hx++)
+              tma_load_2d(sW + ws * WSB + (rb * 2 + hx) * BOXB, tm, (U.nb * 8 + hx * 4) * 8 * BITS,
+                          U.tbeg + s0 + rb * kTcBoxRows, &wfull[ws]);
         }
       }
     }
     __syncwarp();
+  }
+  // with programmatic dependent launch, the next kernel may start launching
+  // once every CTA has finished its units (its CTAs wait for this grid before
+  // they read its output)
+  griddep_launch();
+  if (s_abort) {
+    // a wait gave up: let copies and MMAs already in flight land before the
+    // CTA's shared memory and tensor memory go away
+    const long long t0 = clock64();
+    while (clock64() - t0 < 2000000) {
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -551,9 +637,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
 }
 
 // Split-K combine of the tensor-core kernel's slabs when a block has P > 1
-// chunk groups: one warp per (pass, row, 128-column block) folds the P slabs
-// as a tree, rotates back (FWHT, 1/sqrt(128)), scales by svh and stores y:
-// the same arithmetic, in the same order, as block_epilogue.
+// chunk groups: one warp per (row, 128-column block) folds the P slabs as a
+// tree, rotates back (FWHT, 1/sqrt(128)), scales by svh and stores y: the same
+// arithmetic, in the same order, as block_epilogue.
 struct CombineArgs {
   LinearArgs la;
   int RP;

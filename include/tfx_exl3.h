@@ -95,6 +95,31 @@ int tfx_exl3_group(tfx_exl3_weight* const ws[], int count, const void* x, int ro
 int tfx_exl3_group_into(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
                         const int64_t ldy[], const int col0[], cudaStream_t stream);
 
+/* One step of a chain: a group call (1..3 members of one K, bits and act)
+ * on x, writing ys[i] (rows x ws[i]->N). x is the chain's input or the
+ * output of an earlier step (the next layer of the model consumes it). */
+typedef struct {
+  tfx_exl3_weight* const* ws;
+  int count;
+  const void* x;
+  void* const* ys;
+} tfx_exl3_step;
+
+/* Layer-level chaining (PR #1467, "What this changes": the rotations and the
+ * decode-row linears chained with programmatic dependent launch so that each
+ * launch hides behind the previous one; PR #1475, "What this changes": one
+ * reserve at load, so that a captured decode step allocates and clears
+ * nothing): the steps' launches are enqueued back to back on `stream`, in
+ * order, each step's kernels after the previous step's. With pdl != 0 every
+ * launch carries the programmatic-dependent-launch attribute: a kernel may
+ * start launching while its predecessor finishes, and waits for it
+ * (griddepcontrol.wait) before it reads anything the predecessor wrote; with
+ * pdl == 0 the launches are ordinary stream order. Every step is validated
+ * (shapes, alignment, every member reserved for `rows`) before anything is
+ * enqueued; the chain allocates and clears nothing, so it can be captured in
+ * a CUDA graph. Bytes equal those of the same group calls made one by one. */
+int tfx_exl3_chain(const tfx_exl3_step* steps, int nsteps, int rows, int pdl, cudaStream_t stream);
+
 /* A view of whole 128-column blocks [from, from+n) of w that reads the same
  * stored words and keeps the parent's tile-row stride (PR #1507, "What this
  * changes": exl3.Weight.columns(from, n)). from % 128 == 0, n % 128 == 0,
@@ -217,6 +242,29 @@ int64_t tfx_exl3_debug_set_spin_limit(int64_t clocks);
  * sustains for the rule, the ALU roofline of decode-bound calls. */
 int tfx_exl3_debug_decode_rate(int bits, int tiles_per_warp, float* sink, int* sink_floats, int64_t* weights,
                                cudaStream_t stream);
+
+/* Synthetic trellis encoder: the tail-biting trellis code of each 16x16 tile
+ * whose decoded values are closest (summed squared error) to the targets, by
+ * Viterbi search over the bit-shift trellis of the decode rule with QTIP's
+ * two-pass tail-biting approximation (Tseng et al., 2024). The pages' weights
+ * come from trained checkpoints and show no encoder; this one gives seeded
+ * Gaussian weights a real quantize -> decode error per bit width.
+ * targets : K x N int16, row-major, device: W[k][n] * 128 rounded to an
+ *           integer (the value grid of the decode rule), clamped to
+ *           [-1024, 1023] by the kernel.
+ * trellis : out, device, the tile layout of tfx_exl3_weight with
+ *           tile_row_stride = (N/16)*8*bits; 16-byte aligned.
+ * sq_err  : out, device, one int64 per tile (row-major tile order): the
+ *           tile's summed squared error in grid units^2; may be NULL.
+ * scratch : device, at least tfx_exl3_encode_scratch_bytes(...) bytes (per
+ *           concurrent tile: two 2^16 int32 cost arrays and 256 x 2^(16-bits)
+ *           argmin bytes); 16-byte aligned; caller-owned.
+ * max_ctas: tiles encoded at once (0: one per SM); the scratch size depends on it.
+ * K, N multiples of 16, bits 1..8. Enqueued on `stream`; the words equal the
+ * CPU oracle's bit for bit (all decisions are integer). */
+int tfx_exl3_encode_scratch_bytes(int K, int N, int bits, int max_ctas, size_t* bytes);
+int tfx_exl3_encode(const int16_t* targets, int K, int N, int bits, uint32_t* trellis, int64_t* sq_err, void* scratch,
+                    size_t scratch_bytes, int max_ctas, cudaStream_t stream);
 
 /* Measurement hook: the next linear/group call on this thread records
  * `before` just before its linear-kernel launch and `after` just after it,

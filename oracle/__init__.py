@@ -44,6 +44,13 @@ def lib():
         _lib.exl3o_linear.argtypes = [u32p, ll, i, i, i, dp, dp, dp, i, dp]
         for f in ("exl3o_decode", "exl3o_rot_in", "exl3o_matmul", "exl3o_rot_out", "exl3o_linear"):
             getattr(_lib, f).restype = i
+        ip = C.POINTER(C.c_int)
+        _lib.exl3o_viterbi.argtypes = [i, i, i, ip, ip, i, C.c_uint32, u32p]
+        _lib.exl3o_viterbi.restype = ll
+        _lib.exl3o_encode_tile.argtypes = [ip, i, ip, u32p]
+        _lib.exl3o_encode_tile.restype = ll
+        _lib.exl3o_encode.argtypes = [C.POINTER(C.c_int16), i, i, i, ll, ll, u32p, C.POINTER(ll)]
+        _lib.exl3o_encode.restype = i
     return _lib
 
 
@@ -158,6 +165,63 @@ def linear(trellis, K: int, N: int, bits: int, suh, svh, x, tile_row_stride: int
     _check(lib().exl3o_linear(pt, tile_row_stride, K, N, bits, psu, psv, px, rows,
                               y.ctypes.data_as(C.POINTER(C.c_double))), "linear")
     return y
+
+
+# ---------------------------------------------------------------- trellis encoder
+
+VITERBI_INF = 1 << 30
+
+
+def _i32(a):
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a, a.ctypes.data_as(C.POINTER(C.c_int))
+
+
+def viterbi(W: int, bits: int, val, T, constrain: bool = False, c: int = 0):
+    """Best path of a W-bit shift-register trellis (see exl3_encoder_oracle.c):
+    returns (cost, states)."""
+    v, pv = _i32(val)
+    t, pt = _i32(T)
+    assert v.size == 1 << W
+    st = np.zeros(t.size, dtype=np.uint32)
+    cost = lib().exl3o_viterbi(W, bits, t.size, pv, pt, 1 if constrain else 0, c,
+                               st.ctypes.data_as(C.POINTER(C.c_uint32)))
+    if cost < 0:
+        raise ValueError("oracle viterbi failed")
+    return int(cost), st
+
+
+def state_values() -> np.ndarray:
+    """code_sum(s) - 510 for every 16-bit state (the integer value, units of 1/128)."""
+    return np.array([code_sum(s) - 510 for s in range(1 << 16)], dtype=np.int32)
+
+
+def encode_tile(T, bits: int, val=None):
+    """256 grid targets (stream order) -> (8*bits words, squared error)."""
+    v, pv = _i32(state_values() if val is None else val)
+    t, pt = _i32(T)
+    assert t.size == 256
+    w = np.zeros(8 * bits, dtype=np.uint32)
+    e = lib().exl3o_encode_tile(pt, bits, pv, w.ctypes.data_as(C.POINTER(C.c_uint32)))
+    if e < 0:
+        raise ValueError("oracle encode_tile failed")
+    return w, int(e)
+
+
+def encode(Tgrid, K: int, N: int, bits: int, tile0: int = 0, ntiles: int = 0):
+    """K x N grid targets (int16, units of 1/128) -> (trellis words in the tile
+    layout, squared error over the encoded tiles). Only tiles [tile0, tile0 +
+    ntiles) of the row-major tile order are encoded when ntiles > 0 (the other
+    words stay zero)."""
+    g = np.ascontiguousarray(Tgrid, dtype=np.int16)
+    assert g.shape == (K, N)
+    out = np.zeros((K // 16, (N // 16) * 8 * bits), dtype=np.uint32)
+    err = C.c_longlong()
+    rc = lib().exl3o_encode(g.ctypes.data_as(C.POINTER(C.c_int16)), K, N, bits, tile0, ntiles,
+                            out.ctypes.data_as(C.POINTER(C.c_uint32)), C.byref(err))
+    if rc != 0:
+        raise ValueError(f"oracle encode failed ({rc})")
+    return out, int(err.value)
 
 
 def round_out(y: np.ndarray, dtype: str) -> np.ndarray:

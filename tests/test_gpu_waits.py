@@ -1,4 +1,4 @@
-"""Bounded waits in the decode-rows kernel, made to give up on a healthy GPU.
+"""Bounded waits in the decode-rows and tensor-core kernels, made to give up on a healthy GPU.
 
 Every wait of a kernel on a copy into shared memory polls for at most the
 launch's spin limit (about 1 s by default). Lowering the limit to one clock
@@ -57,6 +57,40 @@ def test_decode_rows_waits_give_up_and_recover(rows):
         again = tfx.linear(w, x)
         torch.cuda.synchronize()
         assert same_bytes(again, good)
+        assert tfx.device_error(w) == 0
+    finally:
+        tfx.set_spin_limit(0)
+        tfx.set_variant(tfx.VARIANT_AUTO)
+
+
+def test_tensor_core_waits_give_up_and_recover():
+    # the tensor-core kernel: every hand-off is an mbarrier polled for at most
+    # the spin limit; a wait that gives up aborts the CTA (device error 1), every
+    # role leaves its loop at its next wait, copies and MMAs in flight land, TMEM
+    # is freed and the launch ends
+    hw, w = make(71, 5120, 1024, 4, max_rows=128)
+    x64, x = x_of(71, 100, 5120)
+    tfx.set_variant(tfx.VARIANT_MID)
+    try:
+        good = tfx.linear(w, x)
+        torch.cuda.synchronize()
+        assert tfx.device_error(w) == 0
+        tfx.set_spin_limit(1)
+        err = 0
+        for _ in range(5):
+            tfx.linear(w, x)
+            torch.cuda.synchronize()
+            err = tfx.device_error(w)
+            if err:
+                break
+        assert err == 1
+        tfx.set_spin_limit(0)
+        tfx.reset_counters(w)  # an aborted launch may leave split-K counters behind
+        assert tfx.device_error(w) == 0
+        for _ in range(3):
+            again = tfx.linear(w, x)
+            torch.cuda.synchronize()
+            assert same_bytes(again, good)
         assert tfx.device_error(w) == 0
     finally:
         tfx.set_spin_limit(0)

@@ -222,13 +222,15 @@ def test_kernel_choice_and_tensor_core_unit_size(L):
         for rows in (33, 48, 64, 65, 100, 128, 129, 4096):
             assert shape(5120, 4, rows, 40, 152)[0] == tfx.FAMILY_TENSOR, rows
         # G on 152 SMs, K = 5120 (16 chunks): 5120 x 5120 (40 blocks), the q/k/v group (64 blocks), gate+up (272)
-        want = {(40, 64): 2, (40, 128): 2, (64, 64): 8, (64, 128): 4, (272, 64): 16, (272, 128): 4}
+        want = {(40, 64): 2, (40, 128): 2, (64, 64): 8, (64, 128): 8, (272, 64): 16, (272, 128): 16}
         for (blocks, rows), g in want.items():
             assert shape(5120, 4, rows, blocks, 152) == (tfx.FAMILY_TENSOR, g), (blocks, rows)
-        # above 128 rows every unit holds all C chunks (64-row passes, no slabs)
+        # above 128 rows every unit holds all C chunks of a 128-row pass (no slabs)
         assert shape(5120, 4, 4096, 136, 152) == (tfx.FAMILY_TENSOR, 16)
         assert shape(1024, 4, 200, 8, 152) == (tfx.FAMILY_TENSOR, 16)
-        # G is a power of two dividing C whose TMEM regions fit: (2 + log2 G) * rows16 <= 512 columns
+        # G is a power of two dividing C whose chunk-tree levels fit: the TMEM
+        # levels next to two accumulator regions of rows16 columns, plus at
+        # most two levels parked in global scratch
         for K in (256, 1024, 5120, 17408):
             c = min(16, K // 64)
             c = 1 << (c.bit_length() - 1)
@@ -238,7 +240,8 @@ def test_kernel_choice_and_tensor_core_unit_size(L):
                         f, g = shape(K, 4, rows, blocks, sms)
                         assert f == tfx.FAMILY_TENSOR
                         assert g >= 1 and g & (g - 1) == 0 and c % g == 0, (K, rows, blocks, sms, g)
-                        assert (2 + g.bit_length() - 1) * ((rows + 15) // 16 * 16) <= 512
+                        tmem_levels = min(4, 512 // ((rows + 15) // 16 * 16) - 2)
+                        assert g.bit_length() - 1 <= tmem_levels + 2
         # forced families
         tfx.set_variant(tfx.VARIANT_MID)
         assert shape(5120, 4, 1, 40, 152)[0] == tfx.FAMILY_TENSOR
