@@ -619,6 +619,29 @@ def run_gpu(args):
                 detail[f"lm_head_{name}_rows{rows}_us"] = round(us, 3)
                 detail[f"lm_head_{name}_rows{rows}_GBps"] = round(nbytes / us / 1e3, 1)
         del head, first, tails, packs, hcodes
+        # trellis encoder: a seeded Gaussian 1024 x 1024 weight (4096 tiles,
+        # std 1.155, the decode rule's value spread) on the value grid; per bit
+        # width the GPU's tiles/s and the decoded weights' mean squared error
+        EK = EN = 1024
+        rng_e = np.random.default_rng(9000 + rank)
+        tg = np.clip(np.rint(rng_e.normal(0.0, 1.155, (EK, EN)) * 128), -1024, 1023).astype(np.int16)
+        t_tg = torch.from_numpy(tg).to(dev)
+        for eb in range(1, 9):
+            scr = torch.empty(tfx.encode_scratch_bytes(EK, EN, eb), dtype=torch.uint8, device=dev)
+            tfx.encode(t_tg, eb, scratch=scr, stream=stream)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            _, err = tfx.encode(t_tg, eb, scratch=scr, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            tiles = (EK // 16) * (EN // 16)
+            detail[f"encode_bits{eb}_tiles_per_s"] = round(tiles / (ms / 1e3), 1)
+            detail[f"encode_bits{eb}_mse"] = round(float(err.sum()) / (EK * EN) / 128 ** 2, 6)
+            del scr
+        del t_tg
+
         gate = tfx.Weight(gbase[0][0], gbase[0][1], gbase[0][2], K, GU, BITS, tfx.BF16)
         tfx.reserve(gate, 4096, stream)
         x4k = torch.from_numpy(synth.activations(4000 + rank, 4096, K, "bf16").view(np.int16)).to(dev).view(torch.bfloat16)
@@ -631,6 +654,15 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = oracle_sample()
+        if not args.no_detail:
+            # the encoder's CPU oracle on a bounded sample: 4 tiles of the same
+            # kind of weight at 4 bits, one core
+            import oracle
+            rng_c = np.random.default_rng(9100)
+            tgc = np.clip(np.rint(rng_c.normal(0.0, 1.155, (32, 32)) * 128), -1024, 1023).astype(np.int16)
+            t0 = time.perf_counter()
+            oracle.encode(tgc, 32, 32, 4)
+            detail["encode_bits4_cpu_oracle_tiles_per_s"] = round(4 / (time.perf_counter() - t0), 3)
 
     if rank == 0:
         line = {

@@ -73,9 +73,7 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__
     mi++;
   }
   if (mi >= a.count) return;
-  const Member& M = a.m[mi];
-  if (M.P <= 1) return;
-  combine_item(a, M, (int)(w / M.NB), (int)(w % M.NB), ca.RP, lane);
+  combine_item(a, a.m[mi], (int)(w / a.m[mi].NB), (int)(w % a.m[mi].NB), ca.RP, lane);
 }
 
 }  // namespace tfx
@@ -585,12 +583,13 @@ size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
     const size_t m = (size_t)(C / rows_gw(C)) * mid * w->N * 4;
     need = m > need ? m : need;
   }
-  // tensor-core slabs: one pass of at most kTcRowsMax rows, at most C slabs;
-  // calls above kTcRowsMax rows keep every chunk in one unit and write none,
-  // but a weight reserved for more rows also serves calls of up to
-  // kTcRowsMax rows, which may split K into slabs
+  // tensor-core slabs: up to kTcRowsMax rows, one pass of at most C slabs;
+  // above that one slab per pass (each unit holds all C chunks), i.e. every
+  // row's z once; a weight reserved for more rows also serves the shorter calls
   const int rp = rows < kTcRowsMax ? rows : kTcRowsMax;
-  const size_t tc = (size_t)C * rp * w->N * 4;
+  size_t tc = (size_t)C * rp * w->N * 4;
+  const size_t whole = (size_t)((rows + kTcRowsNoSpill - 1) / kTcRowsNoSpill) * kTcRowsNoSpill * w->N * 4;
+  if (whole > tc) tc = whole;
   return tc > need ? tc : need;
 }
 
@@ -762,13 +761,14 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
                          : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
   if (rc) return rc;
   if (f.kind == kTensor) {
-    // members split over P > 1 units: fold their slabs, one warp per (row, block)
+    // fold every block's slabs (one, when a unit covered all C chunks), rotate
+    // back and store y: one warp per (row, block)
     CombineArgs ca = {};
     ca.la = la;
     ca.RP = per_pass;
     long long warps = 0;
     for (int i = 0; i < count; i++) {
-      ca.items[i] = la.m[i].P > 1 ? (long long)rows * la.m[i].NB : 0;
+      ca.items[i] = (long long)rows * la.m[i].NB;
       warps += ca.items[i];
     }
     if (warps > 0) {

@@ -22,16 +22,18 @@
 //   warp 21       bulk-copies the x rows of each stage (lanes 0..3, a slice each);
 //   warps 0..15   decode: turn 4 tiles of each stage into FP16 A operands;
 //   warp 20       issues the MMAs strictly in k order (lane 0);
-//   warps 16..19  fold: merge each finished chunk into the chunk tree, then
-//                 write the unit's output: the whole rot_out epilogue when one
-//                 unit covers all C chunks; otherwise the unit's FP32 subtree
-//                 sum goes to its slab, and tc_combine_kernel folds a block's
-//                 slabs afterwards, one warp per (row, block), all in parallel.
-//                 (The pages' form, where the unit that arrives last on the
-//                 block's counter folds the slabs, was built here and measured
-//                 on GB300 at 3-5x the time of a call: one CTA's four fold
-//                 warps then read P x rows x 512 B of slabs from L2 one round
-//                 trip per 4 rows while that CTA's own pipeline waits.)
+//   warps 16..19  fold: merge each finished chunk into the chunk tree and
+//                 write the unit's FP32 subtree sum (the whole z of the block
+//                 when the unit covers all C chunks) to its slab;
+//                 tc_combine_kernel then folds each block's slabs, rotates back
+//                 and stores y, one warp per (row, block), all in parallel.
+//                 Measured on GB300 with timestamps inside the kernel: the
+//                 rot_out epilogue run by the four fold warps at the end of a
+//                 128-row unit took about 54,000 cycles (a third of the unit),
+//                 and the pages' split-K form, where the unit that arrives
+//                 last on the block's counter folds the slabs, made small
+//                 layers 3x slower (one CTA reading P x rows x 512 B of slabs
+//                 one L2 round trip per 4 rows while its pipeline waits).
 // Every hand-off is an mbarrier: full/empty rings for words (copy engine ->
 // decode warps -> word warp), x (copy engine -> MMA warp; MMA completion ->
 // x warp), A buffers (decode warps -> MMA warp; MMA completion -> decode
@@ -70,10 +72,9 @@ constexpr int kTcAB = 2;                              // A (decoded weight) buff
 constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (32 KB)
 constexpr int kTcWRing = 48 * 1024;                   // trellis-word ring
 constexpr int kTcBoxRows = 4;                         // tile rows per word box
-constexpr int kTcExBytes = 2 * 4 * 128 * 4;           // epilogue exchange (two 4-row groups)
 constexpr int kTcMaxLevels = 4;                       // chunk tree levels (C <= 16)
 constexpr int kTcSpillLevels = 2;                     // levels a CTA may park in global scratch
-constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcWRing + kTcExBytes;
+constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcWRing;
 constexpr int kBarFold = 1;  // named barrier of the 4 fold warps (0 is __syncthreads)
 
 // Trellis words of one stage (kTcSK tile rows of a 128-column block) and how
@@ -257,37 +258,6 @@ __device__ __forceinline__ bool wait_lane0(uint64_t* b, uint32_t parity, volatil
   return ok != 0;
 }
 
-// Rows r0..r0+3 of one 128-column block, thread = column n = 32*(warp%4) + lane
-// of the four fold warps: finish the Walsh-Hadamard transform over n in the
-// same stage order as fwht128 (n bits 0..4 across lanes, then bits 5 and 6
-// through shared memory), scale by 1/sqrt(128) and svh, store y (rows below
-// nrows only).
-__device__ __forceinline__ void tc_rot_out_store(float (&v)[4], int n, int lane, float* ex, float sv, const Member& M,
-                                                 long long row0, int ncol, int nrows, int act) {
-#pragma unroll
-  for (int m = 0; m < 5; m++) {
-    const bool hi = (lane >> m) & 1;
-#pragma unroll
-    for (int e = 0; e < 4; e++) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[e], 1 << m);
-      v[e] = hi ? (o - v[e]) : (v[e] + o);
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 4; e++) ex[e * 128 + n] = v[e];
-  fold_bar();
-#pragma unroll
-  for (int e = 0; e < 4; e++) {
-    const float a5 = ex[e * 128 + (n ^ 32)], b = ex[e * 128 + (n ^ 64)], c = ex[e * 128 + (n ^ 96)];
-    const bool h5 = n & 32;
-    const float u0 = h5 ? (a5 - v[e]) : (v[e] + a5);
-    const float u1 = h5 ? (c - b) : (b + c);
-    float o = (n & 64) ? (u1 - u0) : (u0 + u1);
-    o = (o * kInvSqrt128) * sv;
-    if (e < nrows) store_y1(M, act, row0 + e, ncol, o);
-  }
-}
-
 template <int BITS>
 __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_constant__ TcArgs ta) {
   constexpr int kH = kTcSK / 2;  // tiles per decode warp per stage
@@ -299,7 +269,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   unsigned char* sX = dsm;                               // [kTcXS][kTcXStage]
   unsigned char* sA = sX + kTcXS * kTcXStage;            // [kTcAB][kTcAStage]
   unsigned char* sW = sA + kTcAB * kTcAStage;            // [WS][WSB]
-  float* sEx = reinterpret_cast<float*>(sW + kTcWRing);  // [2][4][128]
   __shared__ __align__(8) uint64_t xfull[kTcXS], xdone[kTcXS], afull[kTcAB], adone[kTcAB], wfull[8], wempty[8],
       cdone[2], tfree[2];
   __shared__ uint32_t s_tmem;
@@ -408,12 +377,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     const int lg = warp & 3, n = 32 * lg + lane;
     const uint32_t lane_base = (uint32_t)(lg * 32) << 16;
     float* spill = ta.lev ? ta.lev + (size_t)blockIdx.x * kTcSpillLevels * NMf * 128 + n : nullptr;
-    int gc = -1, exb = 0;
+    int gc = -1;
     bool ok = true;
     for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
       const TcUnit U = tc_unit(ta, u);
       const Member& M = a.m[U.mi];
-      const float sv = __half2float(M.svh[U.nb * 128 + n]);
       const long long slab = (long long)a.rp * M.N;
       for (int c = 0; c < M.G; c++) {
         gc++;
@@ -478,14 +446,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
               float* dst = spill + (size_t)((nlev - ta.tlev) * NMf + cc) * 128;
 #pragma unroll
               for (int e = 0; e < 16; e++) __stcg(dst + e * 128, v[e]);
-            }
-          } else if (M.P == 1) {
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-              float v4[4] = {v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]};
-              tc_rot_out_store(v4, n, lane, sEx + (exb & 1) * 512, sv, M, U.row0 + cc + 4 * q, U.nb * 128 + n,
-                               U.prow - cc - 4 * q, a.act);
-              exb++;
             }
           } else {
             float* part = M.partial + ((long long)U.pass * M.P + U.gidx) * slab + (long long)cc * M.N + U.nb * 128 + n;
