@@ -17,8 +17,9 @@
 // (member, pass, 128-column block, chunk group) in a fixed stride. The work
 // of a unit is cut into stages of kTcSK k-steps that flow through warp roles:
 //   warp 22       asks the tensor copy engine for each stage's trellis words
-//                 (2-D boxes of 4 tile rows x 4 tiles) into a ring of
-//                 tc_word_stages(BITS) stages, as far ahead as the ring allows;
+//                 (2-D boxes of 4 tile rows x 4 tiles, one per lane 0..3) into
+//                 a ring of tc_word_stages(BITS) stages, as far ahead as the
+//                 ring allows;
 //   warp 21       bulk-copies the x rows of each stage (lanes 0..3, a slice each);
 //   warps 0..15   decode: turn 4 tiles of each stage into FP16 A operands;
 //   warp 20       issues the MMAs strictly in k order (lane 0);
@@ -552,9 +553,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     __syncwarp();
   } else {
     // ---------------- trellis words: per stage, 2-D boxes of 4 tiles x 4 tile
-    // rows (two per 4 rows of the stage) into the ring; a slot is refilled
-    // once all 16 decode warps have consumed it
-    if (lane == 0) {
+    // rows (two per 4 rows of the stage) into the ring, one box per lane of
+    // lanes 0..3 (copies issued by one thread complete one after another, so
+    // a stage's boxes come from four threads); a slot is refilled once all 16
+    // decode warps have consumed it
+    if (lane < 4) {
+      constexpr unsigned kMask = 0xFu;
+      const int rb = lane >> 1, hx = lane & 1;
       int gs = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
@@ -562,16 +567,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         const CUtensorMap* tm = &a.tm[U.mi];
         for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
           const int ws = gs % WS;
-          if (gs >= WS) {
-            ok = mbar_wait(&wempty[ws], (uint32_t)((gs - WS) / WS) & 1u, &s_abort, ta.err, spin);
-            if (!ok) break;
-          }
+          int okl = 1;
+          if (lane == 0 && gs >= WS) okl = mbar_wait(&wempty[ws], (uint32_t)((gs - WS) / WS) & 1u, &s_abort, ta.err, spin);
+          ok = __shfl_sync(kMask, okl, 0) != 0;
+          if (!ok) break;
           const int nrb = (min(kTcSK, U.nsteps - s0) + kTcBoxRows - 1) / kTcBoxRows;
-          mbar_expect_tx(&wfull[ws], (uint32_t)(nrb * 2 * BOXB));
-          for (int rb = 0; rb < nrb; rb++)
-            for (int hx = 0; hx < 2; hx++)
-              tma_load_2d(sW + ws * WSB + (rb * 2 + hx) * BOXB, tm, (U.nb * 8 + hx * 4) * 8 * BITS,
-                          U.tbeg + s0 + rb * kTcBoxRows, &wfull[ws]);
+          if (lane == 0) mbar_expect_tx(&wfull[ws], (uint32_t)(nrb * 2 * BOXB));
+          __syncwarp(kMask);
+          if (rb < nrb)
+            tma_load_2d(sW + ws * WSB + (rb * 2 + hx) * BOXB, tm, (U.nb * 8 + hx * 4) * 8 * BITS,
+                        U.tbeg + s0 + rb * kTcBoxRows, &wfull[ws]);
         }
       }
     }
