@@ -706,8 +706,10 @@ def run_case(args):
     """A few calls of one workload on cuda:0 and nothing else (the command the
     ncu captures under profiles/ run): 'qkv_group_rows16' (q/k/v group,
     K = 5120, 4-bit, 16 rows), 'single_5120_rows16' (5120 x 5120, 4-bit, 16
-    rows), 'lm_head_rows1' (5120 x 248,320, 6-bit, 1 row) or 'gate_rows128'
-    (5120 x 17408, 4-bit, 128 rows: the tensor-core kernel)."""
+    rows), 'lm_head_rows1' (5120 x 248,320, 6-bit, 1 row), 'gate_rows128'
+    (5120 x 17408, 4-bit, 128 rows: the tensor-core kernel), 'encode_b4' (the
+    trellis encoder, 1024 x 1024 at 4 bits) or 'decode_rate' (the decode-rate
+    probe)."""
     import numpy as np
     import torch
 
@@ -729,7 +731,22 @@ def run_case(args):
         return out
 
     x = torch.from_numpy(synth.activations(7, 128, K, "f16")).to(dev)
-    if args.case == "gate_rows128":
+    if args.case == "encode_b4":
+        # the trellis encoder on a seeded Gaussian 1024 x 1024 weight at 4 bits
+        rng_e = np.random.default_rng(9000)
+        tg = np.clip(np.rint(rng_e.normal(0.0, 1.155, (1024, 1024)) * 128), -1024, 1023).astype(np.int16)
+        t_tg = torch.from_numpy(tg).to(dev)
+        for i in range(2):
+            words, err = tfx.encode(t_tg, 4)
+        ys = [err.float()]
+    elif args.case == "decode_rate":
+        # the decode-rate probe (the ALU roofline of the bench line)
+        nw, nf = tfx.decode_rate(BITS, 4000)
+        sink = torch.empty(nf, dtype=torch.float32, device=dev)
+        for i in range(3):
+            tfx.decode_rate(BITS, 4000, sink)
+        ys = [sink]
+    elif args.case == "gate_rows128":
         ws_ = weight(8, 17408, BITS, copies=3)
         for w in ws_:
             tfx.reserve(w, 128)
@@ -768,7 +785,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-detail", action="store_true", help="skip the per-row-count detail timings")
-    ap.add_argument("--case", choices=["qkv_group_rows16", "single_5120_rows16", "lm_head_rows1", "gate_rows128"],
+    ap.add_argument("--case", choices=["qkv_group_rows16", "single_5120_rows16", "lm_head_rows1", "gate_rows128",
+                                       "encode_b4", "decode_rate"],
                     help="run a few calls of one workload and exit (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
