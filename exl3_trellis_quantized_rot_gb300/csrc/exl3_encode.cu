@@ -23,8 +23,9 @@
 //     `bits` stream bits are the low bits of its state.
 // The same integer decisions as the CPU oracle, so the words are identical.
 //
-// Work layout: one CTA of 1024 threads per tile at a time (persistent over
-// tiles). The two cost arrays (2^16 int32 each) and the argmins of every step
+// Work layout: one CTA of 512 threads per tile at a time, as many CTAs per SM
+// as fit (persistent over tiles): a tile is a chain of 510 dependent steps, so
+// throughput grows with the tiles in flight. The two cost arrays (2^16 int32 each) and the argmins of every step
 // (2^(16-bits) bytes) live in a per-CTA slice of caller scratch (L2-resident
 // while the tile runs); best[] lives in shared memory.
 #include <cuda_runtime.h>
@@ -36,7 +37,7 @@
 
 namespace tfx {
 
-constexpr int kEncThreads = 1024;
+constexpr int kEncThreads = 512;
 constexpr uint32_t kEncInf = 1u << 30;
 
 struct EncodeArgs {
@@ -159,7 +160,7 @@ __device__ void enc_pass(const int* T, bool constrain, uint32_t c, uint32_t* cos
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_constant__ EncodeArgs a) {
+__global__ void __launch_bounds__(kEncThreads) encode_kernel(const __grid_constant__ EncodeArgs a) {
   constexpr uint32_t NP = 65536u >> BITS;
   constexpr uint32_t m = NP - 1u;
   __shared__ int T[256], R[256];
@@ -238,14 +239,26 @@ const void* encode_kernel_for(int bits) {
 
 namespace {
 
-int enc_ctas(long long tiles, int max_ctas) {
-  int sms = 0, dev = 0;
+// Tiles in flight: every CTA the SMs hold at once (occupancy of the bit
+// width's kernel), at most one per tile, at most max_ctas when given.
+int enc_ctas(long long tiles, int bits, int max_ctas) {
+  int sms = 0, dev = 0, per_sm = 1;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms <= 0) {
     cudaGetLastError();
     sms = 152;
   }
-  long long c = tiles < sms ? tiles : sms;
+  const void* fn = tfx::encode_kernel_for(bits);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tfx::enc_smem_bytes(bits)) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, tfx::kEncThreads, tfx::enc_smem_bytes(bits)) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  long long c = (long long)sms * per_sm;
+  if (tiles < c) c = tiles;
   if (max_ctas > 0 && c > max_ctas) c = max_ctas;
   return (int)(c < 1 ? 1 : c);
 }
@@ -258,7 +271,7 @@ int tfx_exl3_encode_scratch_bytes(int K, int N, int bits, int max_ctas, size_t* 
   if (K <= 0 || N <= 0 || K % 16 || N % 16 || bits < 1 || bits > 8 || !bytes)
     return tfx::report_error(TFX_EINVAL, "encode_scratch_bytes: K, N positive multiples of 16, bits 1..8, bytes");
   const long long tiles = (long long)(K / 16) * (N / 16);
-  *bytes = (size_t)enc_ctas(tiles, max_ctas) * tfx::enc_slice_bytes(bits);
+  *bytes = (size_t)enc_ctas(tiles, bits, max_ctas) * tfx::enc_slice_bytes(bits);
   return 0;
 }
 
@@ -270,7 +283,7 @@ int tfx_exl3_encode(const int16_t* targets, int K, int N, int bits, uint32_t* tr
   if ((reinterpret_cast<uintptr_t>(scratch) | reinterpret_cast<uintptr_t>(trellis)) & 15u)
     return tfx::report_error(TFX_EALIGN, "encode: trellis and scratch must be 16-byte aligned");
   const long long tiles = (long long)(K / 16) * (N / 16);
-  const int ctas = enc_ctas(tiles, max_ctas);
+  const int ctas = enc_ctas(tiles, bits, max_ctas);
   if (scratch_bytes < (size_t)ctas * tfx::enc_slice_bytes(bits))
     return tfx::report_error(TFX_EINVAL, "encode: scratch smaller than tfx_exl3_encode_scratch_bytes");
   tfx::EncodeArgs a;

@@ -16,14 +16,15 @@
 // The kernel is persistent: one CTA per SM walks the work units
 // (member, pass, 128-column block, chunk group) in a fixed stride. The work
 // of a unit is cut into stages of kTcSK k-steps that flow through warp roles:
-//   warp 22       asks the tensor copy engine for each stage's trellis words
+//   warp 14       asks the tensor copy engine for each stage's trellis words
 //                 (2-D boxes of 4 tile rows x 4 tiles, one per lane 0..3) into
 //                 a ring of tc_word_stages(BITS) stages, as far ahead as the
 //                 ring allows;
-//   warp 21       bulk-copies the x rows of each stage (lanes 0..3, a slice each);
-//   warps 0..15   decode: turn 4 tiles of each stage into FP16 A operands;
-//   warp 20       issues the MMAs strictly in k order (lane 0);
-//   warps 16..19  fold: merge each finished chunk into the chunk tree and
+//   warp 13       bulk-copies the x rows of each stage (lanes 0..3, a slice each);
+//   warps 0..7    decode: warp j turns tile column j of each stage (8 tiles)
+//                 into FP16 A operands;
+//   warp 12       issues the MMAs strictly in k order (lane 0);
+//   warps 8..11   fold: merge each finished chunk into the chunk tree and
 //                 write the unit's FP32 subtree sum (the whole z of the block
 //                 when the unit covers all C chunks) to its slab;
 //                 tc_combine_kernel then folds each block's slabs, rotates back
@@ -60,12 +61,12 @@ namespace tfx {
 constexpr int kTcRowsMax = 128;      // rows per pass (MMA N)
 constexpr int kTcRowsNoSpill = 64;   // rows per pass above 128 rows when no level scratch is given
 constexpr int kTcSK = 8;             // k-steps per stage
-constexpr int kTcDecodeWarps = 16;
-constexpr int kTcFoldWarp0 = 16;     // 4 fold warps; TMEM lane quarter = warp % 4
-constexpr int kTcMmaWarp = 20;
-constexpr int kTcXWarp = 21;
-constexpr int kTcWWarp = 22;
-constexpr int kTcThreads = 23 * 32;
+constexpr int kTcDecodeWarps = 8;
+constexpr int kTcFoldWarp0 = 8;      // 4 fold warps; TMEM lane quarter = warp % 4
+constexpr int kTcMmaWarp = 12;
+constexpr int kTcXWarp = 13;
+constexpr int kTcWWarp = 14;
+constexpr int kTcThreads = 15 * 32;
 constexpr int kTcXS = 3;                              // x ring stages
 constexpr int kTcXLanes = 4;                          // lanes that copy a stage's x (one slice each)
 constexpr int kTcXStage = kTcSK * kTcRowsMax * 32;    // x bytes per stage (32 KB)
@@ -261,7 +262,13 @@ __device__ __forceinline__ bool wait_lane0(uint64_t* b, uint32_t parity, volatil
 
 template <int BITS>
 __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_constant__ TcArgs ta) {
-  constexpr int kH = kTcSK / 2;  // tiles per decode warp per stage
+  // tiles per decode warp per stage: one decode warp per tile column, two per
+  // SM sub-partition. Measured on GB300: with 16 decode warps (4 per
+  // sub-partition, 4 tiles each) the single-lane MMA warp, which shares a
+  // sub-partition with always-ready decode warps, took about 770 cycles per
+  // stage for its loop with no MMA issued; 8 decode warps made gate+up at 128
+  // rows 139.5 -> 128.7 us and the 4096-row gate chunk 1880 -> 1717 us.
+  constexpr int kH = kTcSK;
   constexpr int WS = tc_word_stages(BITS);
   constexpr int WSB = tc_word_stage_bytes(BITS);
   constexpr int BOXB = tc_word_box_bytes(BITS);
@@ -326,14 +333,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   const int NMf = ta.NMf;
 
   if (warp < kTcDecodeWarps) {
-    // ---------------- decode: tile column j, k-steps q0 .. q0+kH-1 of every stage
-    const int j = warp & 7, q0 = (warp >> 3) * kH;
+    // ---------------- decode: tile column j, every k-step of every stage
+    const int j = warp & 7, q0 = 0;
     LaneWindow<BITS> lw;
     lw.init(lane);
     const int g = lane >> 2, t = lane & 3;
     const int off0 = 512 * j + 16 * g + 4 * t;  // A-fragment register 0 in the core-matrix layout
-    // tile (q0 + h, j) of a word stage: box (q0/4, j/4), row h, tile j%4
-    const int wofs = ((q0 / kTcBoxRows) * 2 + (j >> 2)) * BOXB + (j & 3) * 32 * BITS;
+    // tile (h, j) of a word stage: box (h/4, j/4), row h%4, tile j%4
+    const int wofs = (j >> 2) * BOXB + (j & 3) * 32 * BITS;
     int gs = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
 #pragma unroll
         for (int h = 0; h < kH; h++) {
           if (q0 + h < cnt) {
-            const uint32_t* tile = reinterpret_cast<const uint32_t*>(wst + h * 128 * BITS);
+            const uint32_t* tile = reinterpret_cast<const uint32_t*>(wst + (h >> 2) * 2 * BOXB + (h & 3) * 128 * BITS);
             uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
             raw[0] = tile[lw.i0];
             raw[1] = tile[lw.i1];
@@ -555,8 +562,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     // ---------------- trellis words: per stage, 2-D boxes of 4 tiles x 4 tile
     // rows (two per 4 rows of the stage) into the ring, one box per lane of
     // lanes 0..3 (copies issued by one thread complete one after another, so
-    // a stage's boxes come from four threads); a slot is refilled once all 16
-    // decode warps have consumed it
+    // a stage's boxes come from four threads); a slot is refilled once every
+    // decode warp has consumed it
     if (lane < 4) {
       constexpr unsigned kMask = 0xFu;
       const int rb = lane >> 1, hx = lane & 1;

@@ -178,6 +178,23 @@ def test_variants_and_row_counts_byte_identical(K, N, act):
         assert_close(to_f64(ref[:, 128 * blk:128 * blk + 128]), want, act, what=f"K={K} N={N} blk={blk}")
 
 
+@pytest.mark.parametrize("rows", [40, 100])
+def test_mid_rows_every_block_against_oracle(rows):
+    # every 128-column block of a 2048 x 1024 layer against the oracle, in every
+    # kernel family that serves the row count (the byte-identity tests compare
+    # families with each other; this checks each of them against the definition)
+    hw, w = make(17, 2048, 1024, 4, act=tfx.BF16, max_rows=128)
+    x64, x = x_of(17, rows, 2048, tfx.BF16)
+    want = oracle_y(hw, x64)
+    try:
+        for var in (tfx.VARIANT_AUTO, tfx.VARIANT_MID, tfx.VARIANT_WARP, tfx.VARIANT_ROWS):
+            tfx.set_variant(var)
+            y = tfx.linear(w, x)
+            assert_close(to_f64(y), want, tfx.BF16, what=f"rows={rows} variant={var}")
+    finally:
+        tfx.set_variant(tfx.VARIANT_AUTO)
+
+
 def test_gate_up_group_mid_rows():
     gate = make(8, 5120, 17408, 4, act=tfx.BF16, member=0, max_rows=128)
     up = make(8, 5120, 17408, 4, act=tfx.BF16, member=1, max_rows=128)
@@ -200,7 +217,7 @@ def test_prefill_4096_rows():
     for r0 in (0, 128, 2048, 3968):
         assert same_bytes(y[r0:r0 + 128], tfx.linear(w, x[r0:r0 + 128]))
     rows = [0, 127, 128, 1000, 2047, 4095]
-    for blk in (0, 100):
+    for blk in (0, 37, 100, 135):
         want = oracle_y(hw, x64[rows], 128 * blk, 128)
         assert_close(to_f64(y[rows][:, 128 * blk:128 * blk + 128]), want, tfx.BF16, what=f"prefill blk={blk}")
 
