@@ -516,8 +516,9 @@ def run_gpu(args):
             tfx.chain([([q, k, v], x, ys), ([o6[i % copies]], ys[0], [yo6])], ROWS, pdl=pdl, stream=stream)
 
         detail["chain_qkv_o_rows16_unchained_us"] = round(time_calls(unchained, n_calls), 3)
-        detail["chain_qkv_o_rows16_pdl_off_us"] = round(time_calls(lambda i: chained(i, False), n_calls), 3)
-        detail["chain_qkv_o_rows16_pdl_on_us"] = round(time_calls(lambda i: chained(i, True), n_calls), 3)
+        detail["chain_qkv_o_rows16_pdl_off_us"] = round(time_calls(lambda i: chained(i, 0), n_calls), 3)
+        detail["chain_qkv_o_rows16_pdl_on_us"] = round(time_calls(lambda i: chained(i, 1), n_calls), 3)
+        detail["chain_qkv_o_rows16_pdl_auto_us"] = round(time_calls(lambda i: chained(i, 2), n_calls), 3)
         del o6, ocodes
 
         # mid rows on the 5120x5120 weight (same copies, reserved for 128 rows)

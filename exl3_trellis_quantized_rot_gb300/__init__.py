@@ -245,10 +245,15 @@ def pack_spans(views, x, out, col0, rows: int | None = None, stream=None):
     return out
 
 
-def chain(steps, rows: int, pdl: bool = True, stream=None):
+def _pdl_mode(pdl) -> int:
+    return (1 if pdl else 0) if isinstance(pdl, bool) else int(pdl)
+
+
+def chain(steps, rows: int, pdl=True, stream=None):
     """Run group calls back to back (tfx_exl3_chain). steps: list of
     (weights, x, ys); a step's x may be an earlier step's output. Outputs
-    must be allocated by the caller (the chain allocates nothing)."""
+    must be allocated by the caller (the chain allocates nothing). pdl:
+    True/1 on every launch, False/0 off, 2 the automatic choice."""
     keep = []
     arr = (StepStruct * len(steps))()
     for st, (ws, x, ys) in zip(arr, steps):
@@ -259,7 +264,7 @@ def chain(steps, rows: int, pdl: bool = True, stream=None):
         st.count = len(ws)
         st.x = _ptr(x)
         st.ys = C.cast(ya, C.POINTER(C.c_void_p))
-    _check(lib().tfx_exl3_chain(arr, len(steps), rows, 1 if pdl else 0, _stream(stream)))
+    _check(lib().tfx_exl3_chain(arr, len(steps), rows, _pdl_mode(pdl), _stream(stream)))
 
 
 def encode_scratch_bytes(K: int, N: int, bits: int, max_ctas: int = 0) -> int:
@@ -351,8 +356,13 @@ def decode_rate(bits: int, tiles_per_warp: int, sink=None, stream=None):
     return nw.value, nf.value
 
 
-def set_pdl(on: bool) -> int:
-    return lib().tfx_exl3_set_pdl(1 if on else 0)
+def set_pdl(mode) -> int:
+    """0/False off, 1/True every launch, 2 automatic (the default). Returns the
+    previous mode."""
+    old = lib().tfx_exl3_set_pdl(_pdl_mode(mode))
+    if old < 0:
+        _check(old)
+    return old
 
 
 def mark_events(before, after) -> None:

@@ -33,11 +33,11 @@ namespace tfx {
 // or in core-matrix order (xc_byte) for the tensor-core kernel. One warp per
 // (row, 128-block); x is read once; rows rows..rows_pad-1 are written as zero.
 __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArgs a) {
-  // wait first, then let the linear kernel launch: triggering before the wait
-  // would let the next call's kernels launch (and hold SM resources) while the
-  // previous call still runs, a cascade across a whole graph of calls
+  // wait first; the linear kernel may launch once every warp has stored its
+  // block (a warp with no block has exited, which counts the same): an early
+  // trigger lets the linear kernel's CTAs hold SM resources while the
+  // rotation still runs (measured slower inside graphs)
   griddep_wait();
-  griddep_launch();
   const int lane = threadIdx.x & 31;
   const long long item = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int nblk = a.K / 128;
@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArg
       *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(a.xf[m]) + xc_byte(r, 128 * b + 4 * lane, a.K, a.rp_tc, a.rows_pad)) = o;
     }
   }
+  griddep_launch();
 }
 
 __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ CombineArgs ca) {
@@ -120,13 +121,19 @@ int env_variant() {
   if (!strcmp(v, "warp")) return 3;
   return 0;
 }
-// Programmatic dependent launch is off unless TFX_EXL3_PDL=1: measured on
-// GB300 inside CUDA graphs, letting the clustered linear kernel launch during
-// the rotation kernel made calls slower (5120 x 1024 at 1 row: 13 us against
-// 8.7 us without it), while outside graphs it mostly hides host launch cost.
+// Programmatic dependent launch: 0 off, 1 on every kernel, 2 (the default)
+// automatic: on the rotation launch and on the decode-rows linear launch that
+// follows it, nowhere else. Measured on GB300 inside CUDA graphs (calls back
+// to back, K = 5120, 4-bit): with it on every kernel a 1-row 5120 x 5120 call
+// (one fused kernel, no rotation launch) takes 14.3 us against 13.0 without;
+// on the rotation and decode-rows launches of 7- and 16-row calls it saves
+// 3-5 % (16 rows: 16.7 -> 16.2 us, q/k/v group 24.3 -> 23.6 us).
+// TFX_EXL3_PDL=0 or 1 overrides the default.
 int env_pdl() {
   const char* v = getenv("TFX_EXL3_PDL");
-  return v && !strcmp(v, "1");
+  if (v && !strcmp(v, "0")) return 0;
+  if (v && !strcmp(v, "1")) return 1;
+  return 2;
 }
 // Process-wide switches: read by every call, written by the set_* hooks.
 std::atomic<int> g_variant{env_variant()};
@@ -271,6 +278,9 @@ int row_tile(int rows) { return rows <= 8 ? 0 : rows <= 16 ? 1 : rows <= 32 ? 2 
 // kernel rotates each CTA's chunk of x itself.
 constexpr int kFuseRotRows = 4;
 constexpr long long kFuseRotWeights = 64LL << 20;
+// Decode-rows launches of more clusters than this arrive early on the closing
+// cluster barrier (LinearArgs::early_arrive).
+constexpr long long kEarlyArriveClusters = 128;
 
 // Kernel choice. auto: up to 32 rows the warp-granular decode-rows kernel,
 // above that the persistent tensor-core kernel (measured on GB300, 4-bit,
@@ -531,7 +541,7 @@ int run(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* c
       sc.lev = pv->lev;
     }
   }
-  return tfx::launch_layer(ws, count, x, rows, ys, ldy, col0, s, sc, g_pdl.load(std::memory_order_relaxed) != 0);
+  return tfx::launch_layer(ws, count, x, rows, ys, ldy, col0, s, sc, g_pdl.load(std::memory_order_relaxed));
 }
 
 int grow(void** p, size_t* have, size_t want, cudaStream_t s, Priv* pv, bool zero) {
@@ -606,7 +616,7 @@ size_t level_bytes_needed(int rows) {
 }
 
 int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
-                 const int64_t* ldy, const int* col0, cudaStream_t s, const Scratch& sc, bool pdl) {
+                 const int64_t* ldy, const int* col0, cudaStream_t s, const Scratch& sc, int pdl) {
   const int K = ws[0]->K, bits = ws[0]->bits;
 
   // rotation of x, once for all members
@@ -718,6 +728,10 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     // us); on large calls the redundant rotation costs more than it saves
     // (LM head at 1 row 444 -> 482 us)
     la.fuse_rot = (rows <= kFuseRotRows && stg.x_whole && weights < kFuseRotWeights) ? 1 : 0;
+    // CTAs leave the closing cluster barrier early only where other clusters
+    // wait for their SM slots (about 54-68 clusters of 16 CTAs are resident
+    // at once on 152 SMs)
+    la.early_arrive = clusters > kEarlyArriveClusters ? 1 : 0;
     la.x = x;
     for (int i = 0; i < count; i++) {
       rc = encode_trellis_map(ws[i], f.ncol * 8 * bits, stg.H, &la.tm[i]);
@@ -747,18 +761,23 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     const long long S = sm_count();
     ctas = ctas < S ? ctas : S;  // persistent: one CTA per SM at most
   }
+  // programmatic dependent launch per kernel (see env_pdl): in the automatic
+  // mode only a decode-rows call with its own rotation launch takes it, on
+  // both of its launches
+  const bool pdl_auto = pdl == 2 && f.kind == kRowsWarp && !la.fuse_rot;
+  const bool pdl_rot = pdl == 1 || pdl_auto, pdl_lin = pdl == 1 || pdl_auto, pdl_comb = pdl == 1;
   // everything that can fail on the host is done: enqueue the rotation, then the linear kernel
   if (!la.fuse_rot) {
     rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
-                pdl);
+                pdl_rot);
     if (rc) return rc;
   }
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && record_event(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
   const int cluster = f.kind == kRowsWarp ? chunks_of(K) : 1;
-  rc = f.kind != kTensor ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl, cluster)
-                         : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl);
+  rc = f.kind != kTensor ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl_lin, cluster)
+                         : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl_lin);
   if (rc) return rc;
   if (f.kind == kTensor) {
     // fold every block's slabs (one, when a unit covered all C chunks), rotate
@@ -773,7 +792,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     }
     if (warps > 0) {
       rc = launch(reinterpret_cast<const void*>(&tc_combine_kernel), dim3((unsigned)((warps + 7) / 8)), dim3(256), 0,
-                  s, &ca, pdl);
+                  s, &ca, pdl_comb);
       if (rc) return rc;
     }
   }
@@ -806,6 +825,7 @@ int tfx_exl3_group_into(tfx_exl3_weight* const ws[], int count, const void* x, i
 
 int tfx_exl3_chain(const tfx_exl3_step* steps, int nsteps, int rows, int pdl, cudaStream_t stream) {
   if (!steps || nsteps < 1) return fail(TFX_EINVAL, "chain of %d steps", nsteps);
+  if (pdl < 0 || pdl > 2) return fail(TFX_EINVAL, "chain pdl mode %d (0, 1 or 2)", pdl);
   // every step is validated (shapes, alignment, reserve) before anything is enqueued
   for (int i = 0; i < nsteps; i++) {
     const tfx_exl3_step& st = steps[i];
@@ -833,7 +853,7 @@ int tfx_exl3_chain(const tfx_exl3_step* steps, int nsteps, int rows, int pdl, cu
         sc.lev = pv->lev;
       }
     }
-    const int rc = tfx::launch_layer(st.ws, st.count, st.x, rows, st.ys, nullptr, nullptr, stream, sc, pdl != 0);
+    const int rc = tfx::launch_layer(st.ws, st.count, st.x, rows, st.ys, nullptr, nullptr, stream, sc, pdl);
     if (rc) return fail(rc, "step %d: %s", i, g_err.c_str());
   }
   return 0;
@@ -953,7 +973,10 @@ int tfx_exl3_set_variant(int variant) {
   return g_variant.exchange(variant);
 }
 
-int tfx_exl3_set_pdl(int on) { return g_pdl.exchange(on ? 1 : 0); }
+int tfx_exl3_set_pdl(int mode) {
+  if (mode < 0 || mode > 2) return fail(TFX_EINVAL, "pdl mode %d (0, 1 or 2)", mode);
+  return g_pdl.exchange(mode);
+}
 
 int64_t tfx_exl3_debug_set_spin_limit(int64_t clocks) {
   return g_spin.exchange(clocks > 0 ? clocks : tfx::kSpinClocks);

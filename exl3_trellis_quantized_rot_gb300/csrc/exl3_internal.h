@@ -32,7 +32,7 @@ size_t level_bytes_needed(int rows);
 // Enqueue the rotation and the linear launch for validated members on `s`;
 // ldy / col0 give each member's output window (null: N and 0).
 int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows, void* const ys[],
-                 const int64_t* ldy, const int* col0, cudaStream_t s, const Scratch& sc, bool pdl);
+                 const int64_t* ldy, const int* col0, cudaStream_t s, const Scratch& sc, int pdl);
 int report_error(int code, const char* msg);
 
 }  // namespace tfx

@@ -90,6 +90,8 @@ struct LinearArgs {
   int x_rows;       // warp-granular kernel: tile rows per x stage (the whole chunk, or H)
   int x_whole;      // warp-granular kernel: 1 if one x stage holds the whole chunk
   int fuse_rot;     // warp-granular kernel: 1 if each CTA rotates its chunk of x itself (few rows)
+  int early_arrive; // warp-granular kernel: 1 to arrive on the closing cluster barrier right after
+                    // the fold's distributed loads (launches of many cluster waves)
   const void* x;    // the call's x (rows x K, act dtype), read when fuse_rot
   CUtensorMap tm[3];  // warp-granular kernel: member m's trellis as a 2-D tensor of uint32
                       // words (columns of the view x K/16 tile rows), box (NCOL*8*BITS, H)
@@ -742,6 +744,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // 16 bytes at the same shared-memory offset in the CTA of cluster rank `rank`
 __device__ __forceinline__ float4 ld_dsmem_f4(const void* local, int rank) {
   uint32_t remote;
@@ -1024,7 +1028,15 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
   // the distributed shared-memory loads of the fold
   if constexpr (NR > 1)
     if (chunk + warp * M.C < a.rows) sv4 = *reinterpret_cast<const uint2*>(M.svh + nb * 128 + 4 * lane);
-  // rows chunk, chunk + C, ... of this block: one warp per row
+  // rows chunk, chunk + C, ... of this block: one warp per row. No CTA of the
+  // cluster may exit while another still reads its shared memory: the closing
+  // cluster barrier. With early_arrive a warp arrives on it as soon as its
+  // last distributed load has returned and waits only at the end, so the
+  // CTAs that fold no row leave (and free their SM slots for the next cluster
+  // wave) while the folding warps rotate and store; measured on GB300 this
+  // helps launches of many waves (LM head at 1 row 455 -> 442 us) and costs
+  // single-wave ones about 0.25 us, so the host sets it per launch
+  bool arrived = a.early_arrive == 0;
   for (int r = chunk + warp * M.C; r < a.rows && !dead; r += W * M.C) {
     float v[4];
     const float* src = park + r * 128 + 4 * lane;
@@ -1035,9 +1047,14 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
       case 8: cluster_fold<8>(src, v); break;
       default: cluster_fold<16>(src, v); break;
     }
+    if (!arrived && r + W * M.C >= a.rows) {
+      cluster_arrive();
+      arrived = true;
+    }
     rot_out_row(v, sv4, M, r, nb * 128 + 4 * lane, a.act, lane);
   }
-  cluster_sync();
+  if (!arrived || a.early_arrive == 0) cluster_arrive();
+  cluster_wait();
 }
 
 // Debug: decode every tile to W[k][n] (FP16). One warp per tile.

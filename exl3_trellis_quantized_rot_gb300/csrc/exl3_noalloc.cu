@@ -103,5 +103,5 @@ extern "C" int tfx_exl3_linear_static(const tfx_exl3_weight* w, const void* x, i
   tfx_exl3_weight wc = *w;
   tfx_exl3_weight* ws[1] = {&wc};
   void* ys[1] = {y};
-  return tfx::launch_layer(ws, 1, x, rows, ys, nullptr, nullptr, stream, sc, false);
+  return tfx::launch_layer(ws, 1, x, rows, ys, nullptr, nullptr, stream, sc, 0);
 }

@@ -110,11 +110,13 @@ typedef struct {
  * launch hides behind the previous one; PR #1475, "What this changes": one
  * reserve at load, so that a captured decode step allocates and clears
  * nothing): the steps' launches are enqueued back to back on `stream`, in
- * order, each step's kernels after the previous step's. With pdl != 0 every
- * launch carries the programmatic-dependent-launch attribute: a kernel may
- * start launching while its predecessor finishes, and waits for it
- * (griddepcontrol.wait) before it reads anything the predecessor wrote; with
- * pdl == 0 the launches are ordinary stream order. Every step is validated
+ * order, each step's kernels after the previous step's. pdl selects the
+ * programmatic-dependent-launch attribute per launch: 1 on every launch (a
+ * kernel may start launching while its predecessor finishes, and waits for
+ * it, griddepcontrol.wait, before it reads anything the predecessor wrote or
+ * writes anything it reads); 2 the library's automatic choice (that of
+ * tfx_exl3_set_pdl mode 2); 0 ordinary stream order. Other values: TFX_EINVAL,
+ * nothing enqueued. Every step is validated
  * (shapes, alignment, every member reserved for `rows`) before anything is
  * enqueued; the chain allocates and clears nothing, so it can be captured in
  * a CUDA graph. Bytes equal those of the same group calls made one by one. */
@@ -200,9 +202,15 @@ int tfx_exl3_set_variant(int variant);
 int tfx_exl3_debug_launch_shape(int K, int bits, int rows, int64_t blocks, int sm_count, int* family,
                                 int* chunks_per_unit);
 
-/* Programmatic dependent launch on (1) or off (0); initial value from
- * TFX_EXL3_PDL=1 (default off). Returns the previous value. */
-int tfx_exl3_set_pdl(int on);
+/* Programmatic dependent launch of the single and group calls (PR #1467,
+ * "What this changes"): 0 off, 1 on every launch, 2 automatic (the default:
+ * on the rotation launch and the decode-rows linear launch of a call that has
+ * both, off for fused-rotation, tensor-core and combine launches, the choice
+ * that measured fastest inside CUDA graphs). Initial value from TFX_EXL3_PDL
+ * ("0" or "1"; unset or anything else: 2). Returns the previous mode, or
+ * TFX_EINVAL for a mode outside 0..2 (nothing changed). The static-scratch
+ * entry point never uses it. */
+int tfx_exl3_set_pdl(int mode);
 
 /* Test hook: replace the allocator and memset used by reserve/release so the
  * host logic runs without a GPU. NULL restores the CUDA runtime. */

@@ -53,7 +53,7 @@ def test_chain_bytes_equal_unchained_calls(rows):
     yo = tfx.linear(o, yq)
     yg, yu = tfx.group([g, u], x)
     yd = tfx.linear(d, yg)
-    for pdl in (False, True):
+    for pdl in (0, 1, 2):
         a = _outs(rows, (6144, 1024, 1024, 5120))
         b = _outs(rows, (17408, 17408, 5120))
         tfx.chain([([q, k, v], x, a[:3]), ([o], a[0], a[3:])], rows, pdl=pdl)
@@ -65,7 +65,7 @@ def test_chain_bytes_equal_unchained_calls(rows):
         assert tfx.device_error(w) == 0
 
 
-@pytest.mark.parametrize("pdl", [False, True])
+@pytest.mark.parametrize("pdl", [0, 1, 2])
 def test_captured_chain_allocates_nothing(pdl):
     rows = 16
     (q, k, v, o), (g, u, d) = _chains(rows)

@@ -205,6 +205,13 @@ def test_variant_and_pdl_switches(L):
     assert tfx.set_variant(old) == tfx.VARIANT_MID
     old = tfx.set_pdl(False)
     assert tfx.set_pdl(old) == 0
+    # three modes; the default (unless TFX_EXL3_PDL overrides it) is automatic
+    if os.environ.get("TFX_EXL3_PDL") not in ("0", "1"):
+        assert old == 2
+    assert tfx.set_pdl(1) == old and tfx.set_pdl(2) == 1 and tfx.set_pdl(old) == 2
+    with pytest.raises(tfx.TfxError):
+        tfx.set_pdl(3)
+    assert tfx.set_pdl(old) == old
 
 
 def test_kernel_choice_and_tensor_core_unit_size(L):
