@@ -309,14 +309,14 @@ Family pick(int bits, int rows) {
 // Tensor-core kernel: rows per pass, and chunks per work unit (G). A pass is
 // up to 128 rows (the MMA's N). With level scratch (a reserved weight) every
 // unit of a call above 128 rows holds all C chunks of a 128-row pass: TMEM
-// keeps the two accumulator regions and the first chunk-tree levels, deeper
-// levels go to the scratch, so each weight is decoded once per 128 rows.
-// Without it (the static-scratch entry point) passes above 128 rows are 64
-// rows, where all levels fit in TMEM. Up to 128 rows, G is the power of two
-// that minimises the persistent CTAs' critical path, ceil(units / SMs) unit
-// lengths plus a fixed per-unit cost of 16 k-steps (pipeline fill and fold;
-// measured on GB300 by forcing each G), among those whose TMEM regions fit
-// when no level scratch is given. Launch shape only: the bits do not depend
+// keeps the two pairs of accumulator regions and the first chunk-tree levels,
+// deeper levels go to the scratch, so each weight is decoded once per 128
+// rows. Without it (the static-scratch entry point) passes above 128 rows are
+// 64 rows, where all levels fit in TMEM. Up to 128 rows, G (at least 2: a unit
+// holds whole chunk pairs) is the power of two that minimises the persistent
+// CTAs' critical path, ceil(units / SMs) unit lengths plus a fixed per-unit
+// cost of 16 k-steps (pipeline fill and fold; measured on GB300 by forcing
+// each G), among those whose levels fit TMEM when no level scratch is given. Launch shape only: the bits do not depend
 // on the pass size or on G.
 int tc_rows_per_pass(int rows, bool spill) {
   return rows <= tfx::kTcRowsMax || spill ? tfx::kTcRowsMax : tfx::kTcRowsNoSpill;
@@ -325,20 +325,21 @@ int tc_passes(int rows, bool spill) {
   const int rp = tc_rows_per_pass(rows, spill);
   return (rows + rp - 1) / rp;
 }
-// Chunk-tree levels a region of nm TMEM columns leaves room for next to the
-// two accumulator regions (at most 4, the levels of 16 chunks).
+// Chunk-tree levels above the pairs that TMEM holds next to the two pairs of
+// accumulator regions of nm columns (at most 3, the levels of 8 pairs).
 int tc_tmem_levels(int nm) {
-  const int l = 512 / nm - 2;
+  const int l = 512 / nm - 4;
   return l < tfx::kTcMaxLevels ? l : tfx::kTcMaxLevels;
 }
 int tc_group(long long blocks, int rows, int C, int TK, long long S, bool spill) {
   if (rows > tfx::kTcRowsMax) return C;
   const int nm = (rows + 15) / 16 * 16;
-  int best = 1;
+  int best = 2;
   long long best_cost = -1;
-  for (int g = C; g >= 1; g /= 2) {
+  for (int g = C; g >= 2; g /= 2) {
+    // a unit holds whole chunk pairs: log2(g) - 1 levels above them
     const int lg = __builtin_ctz(g);
-    if (lg > tc_tmem_levels(nm) + (spill ? tfx::kTcSpillLevels : 0)) continue;
+    if (lg - 1 > tc_tmem_levels(nm) + (spill ? tfx::kTcSpillLevels : 0)) continue;
     const long long units = blocks * (C / g);
     const long long cost = (units + S - 1) / S * ((long long)TK * g / C + 16);
     if (best_cost < 0 || cost < best_cost) {
@@ -610,8 +611,9 @@ size_t counter_bytes_needed(const tfx_exl3_weight* w, int rows) {
 
 size_t level_bytes_needed(int rows) {
   // a tensor-core call parks chunk-tree levels in global scratch only when its
-  // TMEM regions are wider than 80 columns (more than 80 rows per pass)
-  if (rows <= 80) return 0;
+  // TMEM regions are wider than 64 columns (more than 64 rows per pass): up to
+  // 64, TMEM holds all three levels above the pairs next to the four regions
+  if (rows <= 64) return 0;
   return (size_t)sm_count() * kTcSpillLevels * kTcRowsMax * 128 * sizeof(float);
 }
 
@@ -755,7 +757,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   ta.tlev = tc_tmem_levels(ta.NMf);
   ta.err = sc.err;
   ta.lev = sc.lev;
-  if (f.kind == kTensor && __builtin_ctz(tcG) > ta.tlev && !sc.lev)
+  if (f.kind == kTensor && __builtin_ctz(tcG) - 1 > ta.tlev && !sc.lev)
     return fail(TFX_EUNSUPPORTED, "tensor-core launch needs chunk-tree level scratch");
   if (f.kind == kTensor) {
     const long long S = sm_count();

@@ -14,17 +14,25 @@
 // i.e. 128 B between k halves and 256 B between row groups.
 //
 // The kernel is persistent: one CTA per SM walks the work units
-// (member, pass, 128-column block, chunk group) in a fixed stride. The work
-// of a unit is cut into stages of kTcSK k-steps that flow through warp roles:
+// (member, pass, 128-column block, chunk group) in a fixed stride. A unit's
+// chunks go in pairs (2p, 2p+1) whose two MMA chains are issued alternately,
+// each into its own accumulator region: an MMA into the accumulator the
+// previous MMA wrote waits for it (measured on GB300: about 180 cycles per
+// dependent tcgen05.mma whatever N, about 90 when two chains alternate), and
+// the pair's sum is the chunk tree's first level, so the bits do not change.
+// The work of a pair is cut into stages of kTcHalf k-steps of each chunk
+// (kTcSK = 2 kTcHalf slots) that flow through warp roles:
 //   warp 14       asks the tensor copy engine for each stage's trellis words
-//                 (2-D boxes of 4 tile rows x 4 tiles, one per lane 0..3) into
+//                 (2-D boxes of 4 tile rows x 4 tiles, one per lane 0..3: the
+//                 first chunk's rows, then the second's) into
 //                 a ring of tc_word_stages(BITS) stages, as far ahead as the
 //                 ring allows;
-//   warp 13       bulk-copies the x rows of each stage (lanes 0..3, a slice each);
+//   warp 13       bulk-copies the x rows of each stage (two runs, one per
+//                 chunk, two lanes each);
 //   warps 0..7    decode: warp j turns tile column j of each stage (8 tiles)
 //                 into FP16 A operands;
-//   warp 12       issues the MMAs strictly in k order (lane 0);
-//   warps 8..11   fold: merge each finished chunk into the chunk tree and
+//   warp 12       issues the MMAs, each chain strictly in k order (lane 0);
+//   warps 8..11   fold: add each finished pair and merge it into the chunk tree and
 //                 write the unit's FP32 subtree sum (the whole z of the block
 //                 when the unit covers all C chunks) to its slab;
 //                 tc_combine_kernel then folds each block's slabs, rotates back
@@ -39,20 +47,20 @@
 // Every hand-off is an mbarrier: full/empty rings for words (copy engine ->
 // decode warps -> word warp), x (copy engine -> MMA warp; MMA completion ->
 // x warp), A buffers (decode warps -> MMA warp; MMA completion -> decode
-// warps) and the two TMEM accumulator regions (MMA completion -> fold warps;
-// fold warps -> MMA warp). A waiter never falls two phases behind: the next
+// warps) and the two TMEM accumulator region pairs (MMA completion -> fold
+// warps; fold warps -> MMA warp). A waiter never falls two phases behind: the next
 // completion of any of these barriers needs the waiter's own next step first.
 // Every wait is bounded by the launch's spin limit. On a timeout the kernel
 // records device error 1 and every role leaves its loop at its next wait (the
 // waits see the abort flag); before the CTA ends, every thread waits about a
 // millisecond so that copies and MMAs in flight land, then TMEM is freed.
 //
-// The chunk tree parks one partial sum per level (up to log2(16) = 4). TMEM
-// holds two accumulator regions plus the first `tlev` levels of NMf columns
-// each within its 512 columns; deeper levels go to a per-CTA slot of global
-// scratch (L2-resident, written and read back by the same thread). That lets
-// one unit hold all C chunks of a 128-row pass, so each weight is decoded once
-// per 128 rows.
+// The chunk tree parks one partial sum per level above the pairs (up to
+// log2(16) - 1 = 3). TMEM holds two pairs of accumulator regions plus the
+// first `tlev` levels of NMf columns each within its 512 columns; deeper
+// levels go to a per-CTA slot of global scratch (L2-resident, written and read
+// back by the same thread). That lets one unit hold all C chunks of a 128-row
+// pass, so each weight is decoded once per 128 rows.
 #pragma once
 #include "exl3_kernels.cuh"
 
@@ -60,8 +68,9 @@ namespace tfx {
 
 constexpr int kTcRowsMax = 128;      // rows per pass (MMA N)
 constexpr int kTcRowsNoSpill = 64;   // rows per pass above 128 rows when no level scratch is given
-constexpr int kTcSK = 8;             // k-steps per stage
-constexpr int kTcDecodeWarps = 8;
+constexpr int kTcHalf = 4;           // k-steps of each chunk of a pair per stage
+constexpr int kTcSK = 2 * kTcHalf;   // k-step slots per stage
+constexpr int kTcDecodeWarps = 8;    // warp j: tile column j, both chunks of the pair
 constexpr int kTcFoldWarp0 = 8;      // 4 fold warps; TMEM lane quarter = warp % 4
 constexpr int kTcMmaWarp = 12;
 constexpr int kTcXWarp = 13;
@@ -74,8 +83,8 @@ constexpr int kTcAB = 2;                              // A (decoded weight) buff
 constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (32 KB)
 constexpr int kTcWRing = 48 * 1024;                   // trellis-word ring
 constexpr int kTcBoxRows = 4;                         // tile rows per word box
-constexpr int kTcMaxLevels = 4;                       // chunk tree levels (C <= 16)
-constexpr int kTcSpillLevels = 2;                     // levels a CTA may park in global scratch
+constexpr int kTcMaxLevels = 3;                       // chunk tree levels above the pairs (C <= 16)
+constexpr int kTcSpillLevels = 3;                     // levels a CTA may park in global scratch
 constexpr size_t kTcDynSmem = (size_t)kTcXS * kTcXStage + kTcAB * kTcAStage + kTcWRing;
 constexpr int kBarFold = 1;  // named barrier of the 4 fold warps (0 is __syncthreads)
 
@@ -208,7 +217,7 @@ struct TcArgs {
   int units;      // work units of all members
   int RP;         // rows per pass
   int NMf;        // TMEM columns per region: min(RP, rows_pad)
-  int tlev;       // chunk tree levels parked in TMEM; deeper ones go to `lev`
+  int tlev;       // chunk tree levels above the pairs parked in TMEM; deeper ones go to `lev`
   int* err;       // device error word: 1 when a wait timed out, 2 on a short shared-memory launch
   float* lev;     // global scratch for deeper levels: per CTA, kTcSpillLevels x NMf x 128 FP32
 };
@@ -240,6 +249,24 @@ __device__ __forceinline__ TcUnit tc_unit(const TcArgs& ta, int u) {
   return U;
 }
 
+// Chunk pair pp of a unit: chunks c = 2pp, 2pp+1 of its group, first k-steps
+// ta, tb and lengths na, nb (each at least 4), ns stages of kTcHalf k-steps of each.
+struct TcPair {
+  int ta, na, tb, nb, ns;
+};
+__device__ __forceinline__ TcPair tc_pair(const TcArgs& ta_, const Member& M, const TcUnit& U, int pp) {
+  const LinearArgs& a = ta_.la;
+  const int c = U.gidx * M.G + 2 * pp;
+  TcPair P;
+  P.ta = chunk_begin(c, a.TK, M.C);
+  P.tb = chunk_begin(c + 1, a.TK, M.C);
+  const int te = chunk_begin(c + 2, a.TK, M.C);
+  P.na = P.tb - P.ta;
+  P.nb = te - P.tb;
+  P.ns = (max(P.na, P.nb) + kTcHalf - 1) / kTcHalf;
+  return P;
+}
+
 __device__ __forceinline__ void fold_bar() { bar_sync(kBarFold, 128); }
 // All 128 fold threads agree: true only if every one passed ok.
 __device__ __forceinline__ bool fold_all(bool ok) {
@@ -267,8 +294,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   // sub-partition, 4 tiles each) the single-lane MMA warp, which shares a
   // sub-partition with always-ready decode warps, took about 770 cycles per
   // stage for its loop with no MMA issued; 8 decode warps made gate+up at 128
-  // rows 139.5 -> 128.7 us and the 4096-row gate chunk 1880 -> 1717 us.
-  constexpr int kH = kTcSK;
+  // rows 139.5 -> 128.7 us and the 4096-row gate chunk 1880 -> 1717 us (with
+  // chunk pairs, 16 warps one per tile column and chunk: 127.6 -> 145.9 us and
+  // 1668 -> 1889 us).
+  constexpr int kH = kTcSK * 8 / kTcDecodeWarps;  // slots per decode warp per stage
   constexpr int WS = tc_word_stages(BITS);
   constexpr int WSB = tc_word_stage_bytes(BITS);
   constexpr int BOXB = tc_word_box_bytes(BITS);
@@ -294,11 +323,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long spin = a.spin;
-  // TMEM: two accumulator regions plus the parked tree levels kept in TMEM
+  // TMEM: two pairs of accumulator regions plus the parked tree levels kept
+  // in TMEM (log2(G) - 1 levels above the pairs)
   int maxlog = a.m[0].log2G;
   for (int i = 1; i < a.count; i++) maxlog = max(maxlog, a.m[i].log2G);
+  const int maxlev = maxlog - 1;
+  if (maxlev < 0 || (4 + min(maxlev, ta.tlev)) * ta.NMf > 512) {
+    if (threadIdx.x == 0) atomicExch(ta.err, 2);
+    return;
+  }
   uint32_t tmem_cols = 32;
-  while (tmem_cols < (uint32_t)((2 + min(maxlog, ta.tlev)) * ta.NMf)) tmem_cols *= 2;
+  while (tmem_cols < (uint32_t)((4 + min(maxlev, ta.tlev)) * ta.NMf)) tmem_cols *= 2;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -334,7 +369,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
 
   if (warp < kTcDecodeWarps) {
     // ---------------- decode: tile column j, every k-step of every stage
-    const int j = warp & 7, q0 = 0;
+    const int j = warp & 7, q0 = (warp >> 3) * kH;
     LaneWindow<BITS> lw;
     lw.init(lane);
     const int g = lane >> 2, t = lane & 3;
@@ -345,8 +380,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
     bool ok = true;
     for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
       const TcUnit U = tc_unit(ta, u);
-      for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
-        const int cnt = min(kTcSK, U.nsteps - s0);
+      const Member& M = a.m[U.mi];
+      for (int pp = 0; pp < (M.G >> 1) && ok; pp++) {
+      const TcPair P = tc_pair(ta, M, U, pp);
+      for (int s = 0; s < P.ns; s++, gs++) {
+        // slots 0..3: the first chunk's k-steps 4s.., slots 4..7: the second's
+        const int cnta = P.na - kTcHalf * s, cntb = P.nb - kTcHalf * s;
         const int ws = gs % WS, ab = gs % kTcAB;
         ok = wait_lane0(&wfull[ws], (uint32_t)(gs / WS) & 1u, &s_abort, ta.err, spin, lane);
         // buffer ab last held stage gs - kTcAB: its MMAs must have completed
@@ -357,8 +396,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         unsigned char* abuf = sA + ab * kTcAStage;
 #pragma unroll
         for (int h = 0; h < kH; h++) {
-          if (q0 + h < cnt) {
-            const uint32_t* tile = reinterpret_cast<const uint32_t*>(wst + (h >> 2) * 2 * BOXB + (h & 3) * 128 * BITS);
+          if (q0 + h < kTcHalf ? q0 + h < cnta : q0 + h - kTcHalf < cntb) {
+            const int hh = q0 + h;
+            const uint32_t* tile = reinterpret_cast<const uint32_t*>(wst + (hh >> 2) * 2 * BOXB + (hh & 3) * 128 * BITS);
             uint32_t raw[Geo<BITS>::kRaw], win[Geo<BITS>::kNorm + 1], af[4];
             raw[0] = tile[lw.i0];
             raw[1] = tile[lw.i1];
@@ -379,6 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           mbar_arrive(&wempty[ws]);
         }
       }
+      }
     }
   } else if (warp < kTcFoldWarp0 + 4) {
     // ---------------- fold and output: thread = TMEM lane = column n of the block
@@ -391,65 +432,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
       const TcUnit U = tc_unit(ta, u);
       const Member& M = a.m[U.mi];
       const long long slab = (long long)a.rp * M.N;
-      for (int c = 0; c < M.G; c++) {
+      for (int pp = 0; pp < (M.G >> 1); pp++) {
         gc++;
         ok = fold_all(wait_lane0(&cdone[gc & 1], (uint32_t)(gc >> 1) & 1u, &s_abort, ta.err, spin, lane));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * NMf);
-        const bool final = c + 1 == M.G;
-        // the levels this chunk closes: c's trailing one bits (all of them for
-        // the unit's last chunk), the first `tlev` of them in TMEM
+        // the pair's two regions: chunk 2pp, then chunk 2pp+1
+        const uint32_t cur = tmem + lane_base + (uint32_t)((gc & 1) * 2 * NMf);
+        const bool final = pp + 1 == (M.G >> 1);
+        // the levels above the pairs this pair closes: pp's trailing one bits
+        // (all of them for the unit's last pair), the first `tlev` in TMEM
         int nlev = 0;
-        while (nlev < kTcMaxLevels && ((c >> nlev) & 1)) nlev++;
+        while (nlev < kTcMaxLevels && ((pp >> nlev) & 1)) nlev++;
         const int nt = min(nlev, ta.tlev);
-        // 16 columns (rows of the pass) at a time: cur + the levels the tree
-        // prescribes (level 0 first), parked again or written out. The TMEM
-        // loads of a group share one round trip; stores are not waited for
-        // until the chunk is done.
+        // 16 columns (rows of the pass) at a time: the pair's sum + the levels
+        // the tree prescribes (lowest first), parked again or written out. The
+        // TMEM loads of a group share one round trip; stores are not waited
+        // for until the pair is done.
         for (int cc = 0; cc < U.NMp; cc += 16) {
           float v[16];
           {
             uint32_t r0[16], r1[16], r2[16];
             tmem_ld16_async(cur + (uint32_t)cc, r0);
-            if (nt > 0) tmem_ld16_async(tmem + lane_base + (uint32_t)(2 * NMf + cc), r1);
-            if (nt > 1) tmem_ld16_async(tmem + lane_base + (uint32_t)(3 * NMf + cc), r2);
+            tmem_ld16_async(cur + (uint32_t)(NMf + cc), r1);
+            if (nt > 0) tmem_ld16_async(tmem + lane_base + (uint32_t)(4 * NMf + cc), r2);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r0[e]);
+            for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r0[e]) + __uint_as_float(r1[e]);
             if (nt > 0)
 #pragma unroll
-              for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r1[e]) + v[e];
-            if (nt > 1)
-#pragma unroll
               for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r2[e]) + v[e];
-            if (nt > 2) {
-              tmem_ld16_async(tmem + lane_base + (uint32_t)(4 * NMf + cc), r1);
-              if (nt > 3) tmem_ld16_async(tmem + lane_base + (uint32_t)(5 * NMf + cc), r2);
+            if (nt > 1) {
+              tmem_ld16_async(tmem + lane_base + (uint32_t)(5 * NMf + cc), r1);
+              if (nt > 2) tmem_ld16_async(tmem + lane_base + (uint32_t)(6 * NMf + cc), r2);
               tmem_wait_ld();
 #pragma unroll
               for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r1[e]) + v[e];
-              if (nt > 3)
+              if (nt > 2)
 #pragma unroll
                 for (int e = 0; e < 16; e++) v[e] = __uint_as_float(r2[e]) + v[e];
             }
-            // levels parked in global scratch (only chunks that close a level
-            // beyond TMEM's: two of every 16 when two levels are parked there)
-            if (nlev > ta.tlev) {
-              const float* src0 = spill + (size_t)cc * 128;
+            // levels parked in global scratch (only pairs that close a level
+            // beyond TMEM's), lowest first
+            for (int l = ta.tlev; l < nlev; l++) {
+              const float* src = spill + (size_t)((l - ta.tlev) * NMf + cc) * 128;
 #pragma unroll
-              for (int e = 0; e < 16; e++) v[e] = __ldcg(src0 + e * 128) + v[e];
-              if (nlev > ta.tlev + 1) {
-                const float* src = spill + (size_t)(NMf + cc) * 128;
-#pragma unroll
-                for (int e = 0; e < 16; e++) v[e] = __ldcg(src + e * 128) + v[e];
-              }
+              for (int e = 0; e < 16; e++) v[e] = __ldcg(src + e * 128) + v[e];
             }
           }
           if (!final) {
-            // park at level nlev (the first clear bit of c)
+            // park at level nlev (the first clear bit of pp)
             if (nlev < ta.tlev) {
-              tmem_st16_async(tmem + lane_base + (uint32_t)((2 + nlev) * NMf + cc), v);
+              tmem_st16_async(tmem + lane_base + (uint32_t)((4 + nlev) * NMf + cc), v);
             } else {
               float* dst = spill + (size_t)((nlev - ta.tlev) * NMf + cc) * 128;
 #pragma unroll
@@ -469,7 +503,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
       }
     }
   } else if (warp == kTcMmaWarp) {
-    // ---------------- MMA issue, strictly in k order, by lane 0
+    // ---------------- MMA issue by lane 0: per stage the pair's two chains
+    // alternately, each strictly in k order
     if (lane == 0) {
       const uint64_t da0 = umma_desc(sA), db0 = umma_desc(sX);
       int gs = 0, gc = -1;
@@ -478,59 +513,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         const TcUnit U = tc_unit(ta, u);
         const Member& M = a.m[U.mi];
         const uint32_t idesc = umma_idesc(U.NMp);
-        const int log2C = ilog2_pow2(M.C);
-        const int c0 = U.gidx * M.G;
-        int ci = -1, cnext = 0;
-        uint32_t acc = 0, dcol = 0;
-        for (int s0 = 0; s0 < U.nsteps && ok; s0 += kTcSK, gs++) {
-          const int cnt = min(kTcSK, U.nsteps - s0);
-          const int ab = gs % kTcAB, xs = gs % kTcXS;
-          ok = mbar_wait(&afull[ab], (uint32_t)(gs / kTcAB) & 1u, &s_abort, ta.err, spin) &&
-               mbar_wait(&xfull[xs], (uint32_t)(gs / kTcXS) & 1u, &s_abort, ta.err, spin);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
-          const uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
-          const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
-          // the stage's k-steps as runs inside one chunk: a chunk start first
-          // resets the accumulator (and waits until its TMEM region was
-          // folded), then the run issues back to back and, if it ends the
-          // chunk, commits it to the fold warps
-          for (int q = 0; q < cnt;) {
-            if (s0 + q == cnext) {
-              ci++;
-              gc++;
-              acc = 0;
-              dcol = (uint32_t)((gc & 1) * NMf);
-              cnext = (int)(((long long)(c0 + ci + 1) * a.TK) >> log2C) - U.tbeg;  // chunk_begin, C a power of two
-              // the region of chunk gc last held chunk gc-2: it must have been folded
-              if (gc >= 2) {
-                ok = mbar_wait(&tfree[gc & 1], (uint32_t)((gc - 2) >> 1) & 1u, &s_abort, ta.err, spin);
-                if (!ok) break;
-              }
-              tc_fence_after();
+        const uint32_t db_step = (uint32_t)(U.NMp * 32) >> 4;
+        for (int pp = 0; pp < (M.G >> 1) && ok; pp++) {
+          const TcPair P = tc_pair(ta, M, U, pp);
+          gc++;
+          const uint32_t d0 = tmem + (uint32_t)((gc & 1) * 2 * NMf), d1 = d0 + (uint32_t)NMf;
+          for (int s = 0; s < P.ns; s++, gs++) {
+            const int cnta = min(kTcHalf, P.na - kTcHalf * s), cntb = min(kTcHalf, P.nb - kTcHalf * s);
+            const int ab = gs % kTcAB, xs = gs % kTcXS;
+            ok = mbar_wait(&afull[ab], (uint32_t)(gs / kTcAB) & 1u, &s_abort, ta.err, spin) &&
+                 mbar_wait(&xfull[xs], (uint32_t)(gs / kTcXS) & 1u, &s_abort, ta.err, spin);
+            // the pair's regions last held pair gc-2: it must have been folded
+            if (ok && s == 0 && gc >= 2) ok = mbar_wait(&tfree[gc & 1], (uint32_t)((gc - 2) >> 1) & 1u, &s_abort, ta.err, spin);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t da = da0 + (uint64_t)((ab * kTcAStage) >> 4);
+            const uint64_t db = db0 + (uint64_t)((xs * kTcXStage) >> 4);
+#pragma unroll
+            for (int q = 0; q < kTcHalf; q++) {
+              const uint32_t acc = (s > 0 || q > 0) ? 1u : 0u;
+              if (q < cnta) umma_f16(d0, da + (uint64_t)(q * (4096 >> 4)), db + (uint64_t)(q * db_step), idesc, acc);
+              if (q < cntb)
+                umma_f16(d1, da + (uint64_t)((kTcHalf + q) * (4096 >> 4)), db + (uint64_t)((kTcHalf + q) * db_step),
+                         idesc, acc);
             }
-            const int qe = min(cnt, cnext - s0);
-            for (int i = q; i < qe; i++) {
-              umma_f16(tmem + dcol, da + (uint64_t)(i * (4096 >> 4)), db + (uint64_t)(i * db_step), idesc, acc);
-              acc = 1;
-            }
-            if (s0 + qe == cnext) umma_commit(&cdone[gc & 1]);
-            q = qe;
+            if (s + 1 == P.ns) umma_commit(&cdone[gc & 1]);
+            // frees A buffer ab and x slot xs once these MMAs have completed
+            umma_commit(&adone[ab]);
+            umma_commit(&xdone[xs]);
           }
-          if (!ok) break;
-          // frees A buffer ab and x slot xs once these MMAs have completed
-          umma_commit(&adone[ab]);
-          umma_commit(&xdone[xs]);
         }
       }
     }
     __syncwarp();
   } else if (warp == kTcXWarp) {
-    // ---------------- x rows of the pass: one contiguous run per stage, cut
-    // into kTcXLanes slices that as many lanes copy: the bulk copies of one
-    // thread complete one after another (measured on GB300: about one per
-    // 0.45 us whatever their size up to 64 KB), those of different threads overlap
+    // ---------------- x rows of the pass: two contiguous runs per stage (one
+    // per chunk of the pair), each cut into two slices that as many lanes
+    // copy: the bulk copies of one thread complete one after another
+    // (measured on GB300: about one per 0.45 us whatever their size up to 64
+    // KB), those of different threads overlap
     if (lane < kTcXLanes) {
       constexpr unsigned kMask = (1u << kTcXLanes) - 1;
       int gs = 0;
@@ -540,27 +561,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         const Member& M = a.m[U.mi];
         const unsigned char* xsrc =
             reinterpret_cast<const unsigned char*>(M.xf) + (long long)U.pass * ta.RP * a.K * 2;
-        for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
-          const int cnt = min(kTcSK, U.nsteps - s0);
-          const int xs = gs % kTcXS;
-          int okl = 1;
-          if (lane == 0 && gs >= kTcXS)
-            okl = mbar_wait(&xdone[xs], (uint32_t)((gs - kTcXS) / kTcXS) & 1u, &s_abort, ta.err, spin);
-          ok = __shfl_sync(kMask, okl, 0) != 0;
-          if (!ok) break;
-          // bytes = cnt * NMp * 32 is a multiple of 512: every slice is a multiple of 16 bytes
-          const uint32_t bytes = (uint32_t)(cnt * U.NMp * 32), slice = bytes / kTcXLanes;
-          if (lane == 0) mbar_expect_tx(&xfull[xs], bytes);
-          __syncwarp(kMask);
-          bulk_g2s(sX + xs * kTcXStage + lane * slice,
-                   xsrc + (long long)(U.tbeg + s0) * U.NMp * 32 + (long long)lane * slice, slice, &xfull[xs]);
+        for (int pp = 0; pp < (M.G >> 1) && ok; pp++) {
+          const TcPair P = tc_pair(ta, M, U, pp);
+          for (int s = 0; s < P.ns; s++, gs++) {
+            const int cnta = max(0, min(kTcHalf, P.na - kTcHalf * s)), cntb = max(0, min(kTcHalf, P.nb - kTcHalf * s));
+            const int xs = gs % kTcXS;
+            int okl = 1;
+            if (lane == 0 && gs >= kTcXS)
+              okl = mbar_wait(&xdone[xs], (uint32_t)((gs - kTcXS) / kTcXS) & 1u, &s_abort, ta.err, spin);
+            ok = __shfl_sync(kMask, okl, 0) != 0;
+            if (!ok) break;
+            // two runs (the first chunk's k-steps to slots 0.., the second's to
+            // slots kTcHalf..), each cut in two halves: cnt * NMp * 16 bytes, a
+            // multiple of 256
+            if (lane == 0) mbar_expect_tx(&xfull[xs], (uint32_t)((cnta + cntb) * U.NMp * 32));
+            __syncwarp(kMask);
+            const int second = lane >> 1, half = lane & 1;
+            const int cnt = second ? cntb : cnta;
+            if (cnt > 0) {
+              const uint32_t slice = (uint32_t)(cnt * U.NMp * 16);
+              const int t0 = (second ? P.tb : P.ta) + kTcHalf * s;
+              bulk_g2s(sX + xs * kTcXStage + second * kTcHalf * U.NMp * 32 + half * slice,
+                       xsrc + (long long)t0 * U.NMp * 32 + (long long)half * slice, slice, &xfull[xs]);
+            }
+          }
         }
       }
     }
     __syncwarp();
   } else {
     // ---------------- trellis words: per stage, 2-D boxes of 4 tiles x 4 tile
-    // rows (two per 4 rows of the stage) into the ring, one box per lane of
+    // rows (two per chunk of the pair) into the ring, one box per lane of
     // lanes 0..3 (copies issued by one thread complete one after another, so
     // a stage's boxes come from four threads); a slot is refilled once every
     // decode warp has consumed it
@@ -572,18 +603,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
       for (int u = blockIdx.x; u < ta.units && ok; u += gridDim.x) {
         const TcUnit U = tc_unit(ta, u);
         const CUtensorMap* tm = &a.tm[U.mi];
-        for (int s0 = 0; s0 < U.nsteps; s0 += kTcSK, gs++) {
-          const int ws = gs % WS;
-          int okl = 1;
-          if (lane == 0 && gs >= WS) okl = mbar_wait(&wempty[ws], (uint32_t)((gs - WS) / WS) & 1u, &s_abort, ta.err, spin);
-          ok = __shfl_sync(kMask, okl, 0) != 0;
-          if (!ok) break;
-          const int nrb = (min(kTcSK, U.nsteps - s0) + kTcBoxRows - 1) / kTcBoxRows;
-          if (lane == 0) mbar_expect_tx(&wfull[ws], (uint32_t)(nrb * 2 * BOXB));
-          __syncwarp(kMask);
-          if (rb < nrb)
-            tma_load_2d(sW + ws * WSB + (rb * 2 + hx) * BOXB, tm, (U.nb * 8 + hx * 4) * 8 * BITS,
-                        U.tbeg + s0 + rb * kTcBoxRows, &wfull[ws]);
+        const Member& M = a.m[U.mi];
+        for (int pp = 0; pp < (M.G >> 1) && ok; pp++) {
+          const TcPair P = tc_pair(ta, M, U, pp);
+          for (int s = 0; s < P.ns; s++, gs++) {
+            const bool va = P.na > kTcHalf * s, vb = P.nb > kTcHalf * s;
+            const int ws = gs % WS;
+            int okl = 1;
+            if (lane == 0 && gs >= WS) okl = mbar_wait(&wempty[ws], (uint32_t)((gs - WS) / WS) & 1u, &s_abort, ta.err, spin);
+            ok = __shfl_sync(kMask, okl, 0) != 0;
+            if (!ok) break;
+            // box row 0: the first chunk's tile rows ta + 4s.., box row 1: the second's
+            if (lane == 0) mbar_expect_tx(&wfull[ws], (uint32_t)(((va ? 1 : 0) + (vb ? 1 : 0)) * 2 * BOXB));
+            __syncwarp(kMask);
+            if (rb == 0 ? va : vb)
+              tma_load_2d(sW + ws * WSB + (rb * 2 + hx) * BOXB, tm, (U.nb * 8 + hx * 4) * 8 * BITS,
+                          (rb == 0 ? P.ta : P.tb) + kTcHalf * s, &wfull[ws]);
+          }
         }
       }
     }

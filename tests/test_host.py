@@ -235,9 +235,10 @@ def test_kernel_choice_and_tensor_core_unit_size(L):
         # above 128 rows every unit holds all C chunks of a 128-row pass (no slabs)
         assert shape(5120, 4, 4096, 136, 152) == (tfx.FAMILY_TENSOR, 16)
         assert shape(1024, 4, 200, 8, 152) == (tfx.FAMILY_TENSOR, 16)
-        # G is a power of two dividing C whose chunk-tree levels fit: the TMEM
-        # levels next to two accumulator regions of rows16 columns, plus at
-        # most two levels parked in global scratch
+        # G is a power of two dividing C, at least 2 (units hold whole chunk
+        # pairs), whose chunk-tree levels above the pairs fit: the TMEM levels
+        # next to four accumulator regions of rows16 columns, plus at most
+        # three levels parked in global scratch
         for K in (256, 1024, 5120, 17408):
             c = min(16, K // 64)
             c = 1 << (c.bit_length() - 1)
@@ -246,9 +247,9 @@ def test_kernel_choice_and_tensor_core_unit_size(L):
                     for sms in (1, 152, 1000):
                         f, g = shape(K, 4, rows, blocks, sms)
                         assert f == tfx.FAMILY_TENSOR
-                        assert g >= 1 and g & (g - 1) == 0 and c % g == 0, (K, rows, blocks, sms, g)
-                        tmem_levels = min(4, 512 // ((rows + 15) // 16 * 16) - 2)
-                        assert g.bit_length() - 1 <= tmem_levels + 2
+                        assert g >= 2 and g & (g - 1) == 0 and c % g == 0, (K, rows, blocks, sms, g)
+                        tmem_levels = min(3, 512 // ((rows + 15) // 16 * 16) - 4)
+                        assert g.bit_length() - 2 <= tmem_levels + 3
         # forced families
         tfx.set_variant(tfx.VARIANT_MID)
         assert shape(5120, 4, 1, 40, 152)[0] == tfx.FAMILY_TENSOR
