@@ -594,11 +594,12 @@ size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
     const size_t m = (size_t)(C / rows_gw(C)) * mid * w->N * 4;
     need = m > need ? m : need;
   }
-  // tensor-core slabs: up to kTcRowsMax rows, one pass of at most C slabs;
-  // above that one slab per pass (each unit holds all C chunks), i.e. every
-  // row's z once; a weight reserved for more rows also serves the shorter calls
+  // tensor-core slabs: up to kTcRowsMax rows, one pass of at most C/2 slabs
+  // (a unit holds at least one chunk pair); above that one slab per pass
+  // (each unit holds all C chunks), i.e. every row's z once; a weight reserved
+  // for more rows also serves the shorter calls
   const int rp = rows < kTcRowsMax ? rows : kTcRowsMax;
-  size_t tc = (size_t)C * rp * w->N * 4;
+  size_t tc = (size_t)(C / 2) * rp * w->N * 4;
   const size_t whole = (size_t)((rows + kTcRowsNoSpill - 1) / kTcRowsNoSpill) * kTcRowsNoSpill * w->N * 4;
   if (whole > tc) tc = whole;
   return tc > need ? tc : need;
