@@ -45,9 +45,9 @@
 //                 layers 3x slower (one CTA reading P x rows x 512 B of slabs
 //                 one L2 round trip per 4 rows while its pipeline waits).
 // Every hand-off is an mbarrier: full/empty rings for words (copy engine ->
-// decode warps -> word warp), x (copy engine -> MMA warp; MMA completion ->
-// x warp), A buffers (decode warps -> MMA warp; MMA completion -> decode
-// warps) and the two TMEM accumulator region pairs (MMA completion -> fold
+// decode warps -> word warp), the stage slots of x and A together (decode
+// warps and the x copy -> MMA warp; MMA completion -> decode warps and x
+// warp) and the two TMEM accumulator region pairs (MMA completion -> fold
 // warps; fold warps -> MMA warp). A waiter never falls two phases behind: the next
 // completion of any of these barriers needs the waiter's own next step first.
 // Every wait is bounded by the launch's spin limit. On a timeout the kernel
@@ -76,12 +76,18 @@ constexpr int kTcMmaWarp = 12;
 constexpr int kTcXWarp = 13;
 constexpr int kTcWWarp = 14;
 constexpr int kTcThreads = 15 * 32;
-constexpr int kTcXS = 3;                              // x ring stages
+// Stages in flight: x slots and A buffers alike, one barrier pair per slot.
+// Measured on GB300 against separate x (3) and A (2) rings with their own
+// barriers: one wait and one commit fewer per stage for the MMA warp, and the
+// shared memory left for a 64 KB word ring (4 stages in flight at 8 bits; a
+// third slot with a 32 KB ring was 25 % slower at 6-8 bits).
+constexpr int kTcStages = 2;
+constexpr int kTcXS = kTcStages;                      // x ring stages
 constexpr int kTcXLanes = 4;                          // lanes that copy a stage's x (one slice each)
 constexpr int kTcXStage = kTcSK * kTcRowsMax * 32;    // x bytes per stage (32 KB)
-constexpr int kTcAB = 2;                              // A (decoded weight) buffers
+constexpr int kTcAB = kTcStages;                      // A (decoded weight) buffers
 constexpr int kTcAStage = kTcSK * 128 * 32;           // A bytes per stage (32 KB)
-constexpr int kTcWRing = 48 * 1024;                   // trellis-word ring
+constexpr int kTcWRing = 64 * 1024;                   // trellis-word ring
 constexpr int kTcBoxRows = 4;                         // tile rows per word box
 constexpr int kTcMaxLevels = 3;                       // chunk tree levels above the pairs (C <= 16)
 constexpr int kTcSpillLevels = 3;                     // levels a CTA may park in global scratch
@@ -306,7 +312,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
   unsigned char* sX = dsm;                               // [kTcXS][kTcXStage]
   unsigned char* sA = sX + kTcXS * kTcXStage;            // [kTcAB][kTcAStage]
   unsigned char* sW = sA + kTcAB * kTcAStage;            // [WS][WSB]
-  __shared__ __align__(8) uint64_t xfull[kTcXS], xdone[kTcXS], afull[kTcAB], adone[kTcAB], wfull[8], wempty[8],
+  // sfull[i]: stage slot i holds its decoded A (8 decode-warp arrivals) and
+  // its x (the x warp's arrival with the bytes); sdone[i]: the slot's MMAs
+  // have completed (one commit frees both the A buffer and the x slot)
+  __shared__ __align__(8) uint64_t sfull[kTcStages], sdone[kTcStages], wfull[8], wempty[8],
       cdone[2], tfree[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
@@ -337,13 +346,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int i = 0; i < kTcXS; i++) {
-      mbar_init(&xfull[i], 1);
-      mbar_init(&xdone[i], 1);
-    }
-    for (int i = 0; i < kTcAB; i++) {
-      mbar_init(&afull[i], kTcDecodeWarps);
-      mbar_init(&adone[i], 1);
+    for (int i = 0; i < kTcStages; i++) {
+      mbar_init(&sfull[i], kTcDecodeWarps + 1);
+      mbar_init(&sdone[i], 1);
     }
     for (int i = 0; i < WS; i++) {
       mbar_init(&wfull[i], 1);
@@ -389,7 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         ok = wait_lane0(&wfull[ws], (uint32_t)(gs / WS) & 1u, &s_abort, ta.err, spin, lane);
         // buffer ab last held stage gs - kTcAB: its MMAs must have completed
         if (ok && gs >= kTcAB)
-          ok = wait_lane0(&adone[ab], (uint32_t)((gs - kTcAB) / kTcAB) & 1u, &s_abort, ta.err, spin, lane);
+          ok = wait_lane0(&sdone[ab], (uint32_t)((gs - kTcAB) / kTcAB) & 1u, &s_abort, ta.err, spin, lane);
         if (!ok) break;
         const unsigned char* wst = sW + ws * WSB + wofs;
         unsigned char* abuf = sA + ab * kTcAStage;
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&afull[ab]);
+          mbar_arrive(&sfull[ab]);
           mbar_arrive(&wempty[ws]);
         }
       }
@@ -526,8 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
           for (int s = 0; s < P.ns; s++, gs++) {
             const int cnta = min(kTcHalf, P.na - kTcHalf * s), cntb = min(kTcHalf, P.nb - kTcHalf * s);
             const int ab = gs % kTcAB, xs = gs % kTcXS;
-            ok = mbar_wait(&afull[ab], (uint32_t)(gs / kTcAB) & 1u, &s_abort, ta.err, spin) &&
-                 mbar_wait(&xfull[xs], (uint32_t)(gs / kTcXS) & 1u, &s_abort, ta.err, spin);
+            ok = mbar_wait(&sfull[ab], (uint32_t)(gs / kTcStages) & 1u, &s_abort, ta.err, spin);
             // the pair's regions last held pair gc-2: it must have been folded
             if (ok && s == 0 && gc >= 2) ok = mbar_wait(&tfree[gc & 1], (uint32_t)((gc - 2) >> 1) & 1u, &s_abort, ta.err, spin);
             if (!ok) break;
@@ -543,9 +547,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
                          idesc, acc);
             }
             if (s + 1 == P.ns) umma_commit(&cdone[gc & 1]);
-            // frees A buffer ab and x slot xs once these MMAs have completed
-            umma_commit(&adone[ab]);
-            umma_commit(&xdone[xs]);
+            // frees A buffer and x slot ab once these MMAs have completed
+            umma_commit(&sdone[ab]);
           }
         }
       }
@@ -573,13 +576,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
             const int xs = gs % kTcXS;
             int okl = 1;
             if (lane == 0 && gs >= kTcXS)
-              okl = mbar_wait(&xdone[xs], (uint32_t)((gs - kTcXS) / kTcXS) & 1u, &s_abort, ta.err, spin);
+              okl = mbar_wait(&sdone[xs], (uint32_t)((gs - kTcXS) / kTcXS) & 1u, &s_abort, ta.err, spin);
             ok = __shfl_sync(kMask, okl, 0) != 0;
             if (!ok) break;
             // two runs (the first chunk's k-steps to slots 0.., the second's to
             // slots kTcHalf..), each cut in two halves: cnt * NMp * 16 bytes, a
             // multiple of 256
-            if (lane == 0) mbar_expect_tx(&xfull[xs], (uint32_t)((cnta + cntb) * U.NMp * 32));
+            // the x warp's arrival on the stage's barrier, with the bytes to come
+            if (lane == 0) mbar_expect_tx(&sfull[xs], (uint32_t)((cnta + cntb) * U.NMp * 32));
             __syncwarp(kMask);
             const int second = lane >> 1, half = lane & 1;
             const int cnt = second ? cntb : cnta;
@@ -587,7 +591,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) linear_tc_kernel(const __grid_c
               const uint32_t slice = (uint32_t)(cnt * U.NMp * 16);
               const int t0 = (second ? P.tb : P.ta) + kTcHalf * s;
               bulk_g2s(sX + xs * kTcXStage + second * kTcHalf * U.NMp * 32 + half * slice,
-                       xsrc + (long long)t0 * U.NMp * 32 + (long long)half * slice, slice, &xfull[xs]);
+                       xsrc + (long long)t0 * U.NMp * 32 + (long long)half * slice, slice, &sfull[xs]);
             }
           }
         }
