@@ -178,6 +178,36 @@ def test_variants_and_row_counts_byte_identical(K, N, act):
         assert_close(to_f64(ref[:, 128 * blk:128 * blk + 128]), want, act, what=f"K={K} N={N} blk={blk}")
 
 
+@pytest.mark.parametrize("K", [384, 640, 1152])
+def test_tensor_core_partial_stages_and_unequal_chunk_pairs(K):
+    """K whose chunks are not a whole number of 4-k-step stages (384: C = 4
+    chunks of 6 k-steps; 640: C = 8 chunks of 5) or differ in length inside a
+    chunk pair (1152: C = 16 chunks of 4 and 5 k-steps alternately, so a pair's
+    second stage holds no k-step of its first chunk): every family and row
+    count gives the same bytes, and every block matches the oracle."""
+    N = 512
+    C = 16
+    while C > 1 and (K // 16) // C < 4:
+        C //= 2
+    sizes = [((c + 1) * (K // 16)) // C - (c * (K // 16)) // C for c in range(C)]
+    assert any(n % 4 for n in sizes)
+    hw, w = make(31, K, N, 4, act=tfx.BF16, max_rows=200)
+    x64, x = x_of(31, 200, K, tfx.BF16)
+    tfx.set_variant(tfx.VARIANT_AUTO)
+    ref = tfx.linear(w, x)  # 200 rows: two 128-row tensor-core passes
+    try:
+        for rows in (1, 16, 33, 40, 64, 100, 128, 129, 200):
+            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_MID, tfx.VARIANT_WARP, tfx.VARIANT_ROWS):
+                tfx.set_variant(var)
+                y = tfx.linear(w, x[:rows])
+                assert same_bytes(y, ref[:rows]), (K, rows, var)
+    finally:
+        tfx.set_variant(tfx.VARIANT_AUTO)
+    want = oracle_y(hw, x64)
+    assert_close(to_f64(ref), want, tfx.BF16, what=f"K={K}")
+    assert tfx.device_error(w) == 0
+
+
 @pytest.mark.parametrize("rows", [40, 100])
 def test_mid_rows_every_block_against_oracle(rows):
     # every 128-column block of a 2048 x 1024 layer against the oracle, in every
