@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libtfx_exl3.so")
 
 OK, EINVAL, ENOTRESERVED, EUNSUPPORTED, EALIGN, ECUDA = 0, -1, -2, -3, -4, -5
 F16, BF16 = 0, 1
-VARIANT_AUTO, VARIANT_ROWS, VARIANT_MID, VARIANT_WARP = 0, 1, 2, 3
+VARIANT_AUTO, VARIANT_ROWS, VARIANT_MID, VARIANT_WARP, VARIANT_WARP_GLOBAL = 0, 1, 2, 3, 4
 
 ABI_SYMBOLS = ("tfx_exl3_linear", "tfx_exl3_group", "tfx_exl3_columns", "tfx_exl3_reserve",
                "tfx_exl3_release", "tfx_exl3_reset_counters", "tfx_exl3_debug_decode", "tfx_exl3_plan",

@@ -119,6 +119,7 @@ int env_variant() {
   if (!strcmp(v, "rows")) return 1;
   if (!strcmp(v, "mid")) return 2;
   if (!strcmp(v, "warp")) return 3;
+  if (!strcmp(v, "warp_global")) return 4;
   return 0;
 }
 // Programmatic dependent launch: 0 off, 1 on every kernel, 2 (the default)
@@ -281,6 +282,22 @@ constexpr long long kFuseRotWeights = 64LL << 20;
 // Decode-rows launches of more clusters than this arrive early on the closing
 // cluster barrier (LinearArgs::early_arrive).
 constexpr long long kEarlyArriveClusters = 128;
+// The decode-rows kernel folds a block's chunk sums through global slabs and
+// the block's counter instead of its cluster's distributed shared memory for
+// launches of many cluster waves at few rows, where CTAs waiting at the
+// cluster barrier for their slowest chunk hold SM slots the next clusters
+// need. Measured on GB300 (graph-replayed, K = 5120, 1 / 4 / 8 rows): 40
+// blocks 12.6 / 14.1 / 14.2 us with the cluster fold against 14.1 / 16.7 /
+// 20.8 us global; 272 blocks 53.8 / 54.7 / 55.1 against 49.5 / 51.7 / 57.4;
+// 768 blocks (6-bit) 174 / 175 / 176 against 149 / 152 / 158; the 6-bit LM
+// head (1940 blocks) 424 / 427 / 429 against 358 / 364 / 374. Variant 4
+// forces it for every decode-rows call of up to kFoldGlobalRows rows.
+constexpr int kFoldGlobalRows = 8;
+bool use_fold_global(int rows, long long blocks) {
+  if (rows > kFoldGlobalRows) return false;
+  if (g_variant.load(std::memory_order_relaxed) == 4) return true;
+  return (rows <= 4 && blocks > 128) || blocks > 512;
+}
 
 // Kernel choice. auto: up to 32 rows the warp-granular decode-rows kernel,
 // above that the persistent tensor-core kernel (measured on GB300, 4-bit,
@@ -299,7 +316,8 @@ Family pick(int bits, int rows) {
   switch (g_variant.load(std::memory_order_relaxed)) {
     case 1: return rows <= tfx::kRowsMaxRows ? rowsk : tc;
     case 2: return tc;
-    case 3: return rows <= tfx::kRowsMaxRows ? warpk : tc;
+    case 3:
+    case 4: return rows <= tfx::kRowsMaxRows ? warpk : tc;
     default:
       if (rows <= 32) return warpk;
       return tc;
@@ -600,6 +618,9 @@ size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
   // for more rows also serves the shorter calls
   const int rp = rows < kTcRowsMax ? rows : kTcRowsMax;
   size_t tc = (size_t)(C / 2) * rp * w->N * 4;
+  // decode-rows global fold: one slab per chunk, up to kFoldGlobalRows rows
+  const size_t fg = (size_t)C * (rows < kFoldGlobalRows ? rows : kFoldGlobalRows) * w->N * 4;
+  if (fg > tc) tc = fg;
   const size_t whole = (size_t)((rows + kTcRowsNoSpill - 1) / kTcRowsNoSpill) * kTcRowsNoSpill * w->N * 4;
   if (whole > tc) tc = whole;
   return tc > need ? tc : need;
@@ -658,6 +679,9 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   la.spin = g_spin.load(std::memory_order_relaxed);
   long long ctas = 0;
   int tcG = 0;
+  long long all_blocks = 0;
+  for (int i = 0; i < count; i++) all_blocks += ws[i]->N / 128;
+  const bool fold_global = f.kind == kRowsWarp && use_fold_global(rows, all_blocks);
   if (f.kind == kTensor) {
     long long blocks = 0;
     for (int i = 0; i < count; i++) blocks += ws[i]->N / 128;
@@ -685,8 +709,8 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
       // cluster that folds the chunk sums in distributed shared memory
       m.G = 1;
       m.TC = f.ncol;
-      m.P = 1;
-      m.arrivals = 0;
+      m.P = fold_global ? m.C : 1;  // slabs of a block: one per chunk with the global fold
+      m.arrivals = fold_global ? m.C : 0;
       ctas += (long long)m.NB * m.C;
     } else if (f.kind == kRowsCta) {
       const int TN = w->N / 16;
@@ -735,6 +759,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     // wait for their SM slots (about 54-68 clusters of 16 CTAs are resident
     // at once on 152 SMs)
     la.early_arrive = clusters > kEarlyArriveClusters ? 1 : 0;
+    la.fold_global = fold_global ? 1 : 0;
     la.x = x;
     for (int i = 0; i < count; i++) {
       rc = encode_trellis_map(ws[i], f.ncol * 8 * bits, stg.H, &la.tm[i]);
@@ -778,7 +803,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && record_event(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
-  const int cluster = f.kind == kRowsWarp ? chunks_of(K) : 1;
+  const int cluster = f.kind == kRowsWarp && !fold_global ? chunks_of(K) : 1;
   rc = f.kind != kTensor ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl_lin, cluster)
                          : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl_lin);
   if (rc) return rc;
@@ -972,7 +997,7 @@ int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets) 
 }
 
 int tfx_exl3_set_variant(int variant) {
-  if (variant < 0 || variant > 3) return g_variant.load();
+  if (variant < 0 || variant > 4) return g_variant.load();
   return g_variant.exchange(variant);
 }
 

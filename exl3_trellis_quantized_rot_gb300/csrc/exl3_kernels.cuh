@@ -90,6 +90,8 @@ struct LinearArgs {
   int x_rows;       // warp-granular kernel: tile rows per x stage (the whole chunk, or H)
   int x_whole;      // warp-granular kernel: 1 if one x stage holds the whole chunk
   int fuse_rot;     // warp-granular kernel: 1 if each CTA rotates its chunk of x itself (few rows)
+  int fold_global;  // warp-granular kernel: 1 to fold a block's chunk sums through global slabs and
+                    // the block's counter (no cluster), 0 in the cluster's distributed shared memory
   int early_arrive; // warp-granular kernel: 1 to arrive on the closing cluster barrier right after
                     // the fold's distributed loads (launches of many cluster waves)
   const void* x;    // the call's x (rows x K, act dtype), read when fuse_rot
@@ -822,7 +824,7 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
   extern __shared__ unsigned char wsm[];
   __shared__ __align__(8) uint64_t wfull[W][2];
   __shared__ __align__(8) uint64_t xfull[2], xempty[2];
-  __shared__ int s_dead;
+  __shared__ int s_dead, s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long cta = blockIdx.x;
   int mi = 0;
@@ -1004,6 +1006,37 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
     const long long w0 = clock64();
     while (clock64() - w0 < 2000000) {
     }
+  }
+  if (a.fold_global) {
+    // the launch has no clusters: this chunk's sums go to the block's slab
+    // [chunk][row][N] and the block's last CTA to arrive on its counter folds
+    // the C slabs in chunk order (the same balanced tree), rotates back, stores
+    // y and resets the counter (PR #1475's split-K form); no CTA waits for
+    // another, so launches of many cluster waves keep their SM slots busy
+    if (!dead) {
+      float* slab = M.partial + (long long)chunk * a.rp * M.N + nb * 128;
+      const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+      for (int c = 0; c < NCOL; c++)
+#pragma unroll
+        for (int q = 0; q < NR; q++) {
+          const int r0 = 8 * q + 2 * t;
+          float* pc = slab + (warp * NCOL + c) * 16 + g;
+          if (r0 < a.rows) {
+            __stcg(pc + (long long)r0 * M.N, acc[c][q][0]);
+            __stcg(pc + (long long)r0 * M.N + 8, acc[c][q][2]);
+          }
+          if (r0 + 1 < a.rows) {
+            __stcg(pc + (long long)(r0 + 1) * M.N, acc[c][q][1]);
+            __stcg(pc + (long long)(r0 + 1) * M.N + 8, acc[c][q][3]);
+          }
+        }
+    }
+    if (arrive_last(M.counters + nb, M.C, &s_last)) {
+      block_epilogue(M, a, 0, nb, a.rows, 0, warp, W, lane);
+      if (threadIdx.x == 0) M.counters[nb] = 0;
+    }
+    return;
   }
   // park the chain sums: park[r][128] FP32, lane (g, t) holds (row 8q + 2t | +1,
   // column g | g + 8) of tile-column warp*NCOL + c

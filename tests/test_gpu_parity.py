@@ -97,12 +97,14 @@ def test_group_planted_controls_go_red(qkv, rows):
     assert not same_bytes(bad[2], ref[2])
 
 
-@pytest.mark.parametrize("variant", [tfx.VARIANT_ROWS, tfx.VARIANT_AUTO])
+@pytest.mark.parametrize("variant", [tfx.VARIANT_ROWS, tfx.VARIANT_AUTO, tfx.VARIANT_WARP_GLOBAL])
 def test_repeated_calls_need_no_memset(variant):
     # VARIANT_ROWS: every block goes through the in-kernel arrival counters (8 splits);
-    # VARIANT_AUTO: the cluster of a block folds its chunk sums in shared memory
+    # VARIANT_AUTO: the cluster of a block folds its chunk sums in shared memory;
+    # VARIANT_WARP_GLOBAL (8 rows): the decode-rows kernel's 16 chunk slabs per
+    # block, summed by the last CTA to arrive on the block's counter
     hw, w = make(4, 5120, 1024, 4)
-    x64, x = x_of(4, 16, 5120)
+    x64, x = x_of(4, 8 if variant == tfx.VARIANT_WARP_GLOBAL else 16, 5120)
     tfx.set_variant(variant)
     try:
         first = tfx.linear(w, x)
@@ -166,7 +168,8 @@ def test_variants_and_row_counts_byte_identical(K, N, act):
     ref = tfx.linear(w, x)  # 128 rows: mid kernel, NR = 16
     try:
         for rows in (1, 3, 4, 5, 7, 16, 17, 24, 32, 33, 48, 49, 64, 100, 128):
-            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP):
+            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP,
+                        tfx.VARIANT_WARP_GLOBAL):
                 tfx.set_variant(var)
                 y = tfx.linear(w, x[:rows])
                 assert same_bytes(y, ref[:rows]), (rows, var)
@@ -197,7 +200,8 @@ def test_tensor_core_partial_stages_and_unequal_chunk_pairs(K):
     ref = tfx.linear(w, x)  # 200 rows: two 128-row tensor-core passes
     try:
         for rows in (1, 16, 33, 40, 64, 100, 128, 129, 200):
-            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_MID, tfx.VARIANT_WARP, tfx.VARIANT_ROWS):
+            for var in (tfx.VARIANT_AUTO, tfx.VARIANT_MID, tfx.VARIANT_WARP, tfx.VARIANT_ROWS,
+                        tfx.VARIANT_WARP_GLOBAL):
                 tfx.set_variant(var)
                 y = tfx.linear(w, x[:rows])
                 assert same_bytes(y, ref[:rows]), (K, rows, var)
@@ -318,7 +322,8 @@ def test_lm_head_span_packing_equals_full_head():
         assert same_bytes(packed[:, 98304:], full[:, 240128 + 7904:])
 
 
-@pytest.mark.parametrize("variant", [tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP])
+@pytest.mark.parametrize("variant", [tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP,
+                                     tfx.VARIANT_WARP_GLOBAL])
 def test_output_window_bytes_equal_plain_call(variant):
     # a member's output window (row stride, first stored column) changes where
     # elements land, never their bytes; columns below col0 and the padding of
@@ -369,7 +374,7 @@ def test_nan_and_inf_reach_their_rows_only():
     xb[2, 5] = float("nan")
     xb[3, 700] = float("inf")
     xb[5, 1] = float("-inf")
-    for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP):
+    for var in (tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_MID, tfx.VARIANT_WARP, tfx.VARIANT_WARP_GLOBAL):
         tfx.set_variant(var)
         try:
             y = tfx.linear(w, xb)

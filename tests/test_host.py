@@ -259,6 +259,11 @@ def test_kernel_choice_and_tensor_core_unit_size(L):
         tfx.set_variant(tfx.VARIANT_ROWS)
         assert shape(5120, 4, 64, 40, 152) == (tfx.FAMILY_ROWS_CTA, 0)
         assert shape(5120, 4, 65, 40, 152)[0] == tfx.FAMILY_TENSOR
+        tfx.set_variant(tfx.VARIANT_WARP_GLOBAL)
+        assert shape(5120, 4, 8, 40, 152) == (tfx.FAMILY_ROWS_WARP, 0)
+        assert shape(5120, 4, 65, 40, 152)[0] == tfx.FAMILY_TENSOR
+        # a value outside 0..4 changes nothing
+        assert tfx.set_variant(5) == tfx.VARIANT_WARP_GLOBAL
     finally:
         tfx.set_variant(old)
     for bad in ((100, 4, 1, 1, 152), (5120, 0, 1, 1, 152), (5120, 9, 1, 1, 152), (5120, 4, 0, 1, 152),

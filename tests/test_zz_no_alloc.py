@@ -37,13 +37,14 @@ def _call_static(w, x, rows, y):
                                     torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("variant", [tfx.VARIANT_AUTO, tfx.VARIANT_ROWS])
+@pytest.mark.parametrize("variant", [tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_WARP_GLOBAL])
 @pytest.mark.parametrize("K,N,bits,rows,act", [(5120, 5120, 4, 16, tfx.F16), (5120, 1024, 3, 7, tfx.F16),
                                                (1024, 2048, 4, 40, tfx.BF16)])
 def test_static_entry_matches_linear_on_two_calls(K, N, bits, rows, act, variant):
     # VARIANT_ROWS sends 1..64 rows through the kernel whose split-K partials are
-    # summed by the last CTA to arrive on each block's counter: the counters and
-    # the error word the static call clears at its start are then in use
+    # summed by the last CTA to arrive on each block's counter, VARIANT_WARP_GLOBAL
+    # up to 8 rows through the decode-rows kernel's global-slab fold: the counters
+    # and the error word the static call clears at its start are then in use
     hw, w = make(40 + bits, K, N, bits, act=act, max_rows=rows)
     ref_w = w
     # a second descriptor of the same weight that was never reserved: the static
