@@ -282,21 +282,29 @@ constexpr long long kFuseRotWeights = 64LL << 20;
 // Decode-rows launches of more clusters than this arrive early on the closing
 // cluster barrier (LinearArgs::early_arrive).
 constexpr long long kEarlyArriveClusters = 128;
-// The decode-rows kernel folds a block's chunk sums through global slabs and
-// the block's counter instead of its cluster's distributed shared memory for
-// launches of many cluster waves at few rows, where CTAs waiting at the
-// cluster barrier for their slowest chunk hold SM slots the next clusters
-// need. Measured on GB300 (graph-replayed, K = 5120, 1 / 4 / 8 rows): 40
-// blocks 12.6 / 14.1 / 14.2 us with the cluster fold against 14.1 / 16.7 /
-// 20.8 us global; 272 blocks 53.8 / 54.7 / 55.1 against 49.5 / 51.7 / 57.4;
-// 768 blocks (6-bit) 174 / 175 / 176 against 149 / 152 / 158; the 6-bit LM
-// head (1940 blocks) 424 / 427 / 429 against 358 / 364 / 374. Variant 4
-// forces it for every decode-rows call of up to kFoldGlobalRows rows.
+// How the decode-rows kernel folds a block's chunk sums (LinearArgs::fold_mode).
+// In the block's cluster every CTA waits at the cluster barrier for its
+// slowest chunk while holding its SM slot; with many blocks that wait is what
+// the next clusters queue behind. Global slabs folded by the combine kernel
+// (one warp per row and block) free every CTA as soon as its chain is done.
+// Measured on GB300 (graph-replayed, K = 5120; cluster / counter / combine):
+//   40 blocks, 1 / 4 / 8 / 16 rows: 12.6 / 13.9 / 14.2 / 16.1 us with the
+//     cluster, 14.1 / 16.7 / 20.8 / 29.8 with the counter, 13.9 / 15.8 / 15.6
+//     / 17.1 with the combine kernel;
+//   the q/k/v group (64 blocks) at 1 / 7 / 16 rows: 17.3 / 20.0 / 23.3 with
+//     the cluster, 18.2 / 19.8 / 21.9 with the combine kernel;
+//   272 blocks at 1 / 4 / 8 rows: 53.8 / 54.6 / 55.2, 49.6 / 51.4 / 55.0,
+//     49.0 / 49.3 / 50.0; gate+up at 16 rows 65.8 against 58.5 combined;
+//   768 blocks (6-bit), 1 / 4 / 8 rows: 177 / 178 / 180, 149 / 152 / 158,
+//     147 / 148 / 151; the 6-bit LM head (1940 blocks): 433 / 435 / 438,
+//     358 / 364 / 374, 352 / 361 / 371.
+// The last-arriver counter form (PR #1475) is the forced variant 4 (up to
+// kFoldGlobalRows rows).
 constexpr int kFoldGlobalRows = 8;
-bool use_fold_global(int rows, long long blocks) {
-  if (rows > kFoldGlobalRows) return false;
-  if (g_variant.load(std::memory_order_relaxed) == 4) return true;
-  return (rows <= 4 && blocks > 128) || blocks > 512;
+int fold_mode_for(int rows, long long blocks) {
+  if (g_variant.load(std::memory_order_relaxed) == 4 && rows <= kFoldGlobalRows) return tfx::kFoldCounter;
+  if (blocks > 128 || (blocks > 48 && rows > 8)) return tfx::kFoldCombine;
+  return tfx::kFoldCluster;
 }
 
 // Kernel choice. auto: up to 32 rows the warp-granular decode-rows kernel,
@@ -618,8 +626,9 @@ size_t partial_bytes_needed(const tfx_exl3_weight* w, int rows) {
   // for more rows also serves the shorter calls
   const int rp = rows < kTcRowsMax ? rows : kTcRowsMax;
   size_t tc = (size_t)(C / 2) * rp * w->N * 4;
-  // decode-rows global fold: one slab per chunk, up to kFoldGlobalRows rows
-  const size_t fg = (size_t)C * (rows < kFoldGlobalRows ? rows : kFoldGlobalRows) * w->N * 4;
+  // decode-rows folds through global slabs: one slab per chunk, every row the
+  // decode-rows kernel serves
+  const size_t fg = (size_t)C * (rows < kRowsMaxRows ? rows : kRowsMaxRows) * w->N * 4;
   if (fg > tc) tc = fg;
   const size_t whole = (size_t)((rows + kTcRowsNoSpill - 1) / kTcRowsNoSpill) * kTcRowsNoSpill * w->N * 4;
   if (whole > tc) tc = whole;
@@ -681,7 +690,8 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   int tcG = 0;
   long long all_blocks = 0;
   for (int i = 0; i < count; i++) all_blocks += ws[i]->N / 128;
-  const bool fold_global = f.kind == kRowsWarp && use_fold_global(rows, all_blocks);
+  const int fold_mode = f.kind == kRowsWarp ? fold_mode_for(rows, all_blocks) : tfx::kFoldCluster;
+  const bool fold_global = fold_mode != tfx::kFoldCluster;
   if (f.kind == kTensor) {
     long long blocks = 0;
     for (int i = 0; i < count; i++) blocks += ws[i]->N / 128;
@@ -710,7 +720,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
       m.G = 1;
       m.TC = f.ncol;
       m.P = fold_global ? m.C : 1;  // slabs of a block: one per chunk with the global fold
-      m.arrivals = fold_global ? m.C : 0;
+      m.arrivals = fold_mode == tfx::kFoldCounter ? m.C : 0;
       ctas += (long long)m.NB * m.C;
     } else if (f.kind == kRowsCta) {
       const int TN = w->N / 16;
@@ -759,7 +769,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
     // wait for their SM slots (about 54-68 clusters of 16 CTAs are resident
     // at once on 152 SMs)
     la.early_arrive = clusters > kEarlyArriveClusters ? 1 : 0;
-    la.fold_global = fold_global ? 1 : 0;
+    la.fold_mode = fold_mode;
     la.x = x;
     for (int i = 0; i < count; i++) {
       rc = encode_trellis_map(ws[i], f.ncol * 8 * bits, stg.H, &la.tm[i]);
@@ -793,7 +803,8 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   // mode only a decode-rows call with its own rotation launch takes it, on
   // both of its launches
   const bool pdl_auto = pdl == 2 && f.kind == kRowsWarp && !la.fuse_rot;
-  const bool pdl_rot = pdl == 1 || pdl_auto, pdl_lin = pdl == 1 || pdl_auto, pdl_comb = pdl == 1;
+  const bool pdl_rot = pdl == 1 || pdl_auto, pdl_lin = pdl == 1 || pdl_auto;
+  const bool pdl_comb = pdl == 1 || (pdl == 2 && fold_mode == tfx::kFoldCombine);
   // everything that can fail on the host is done: enqueue the rotation, then the linear kernel
   if (!la.fuse_rot) {
     rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,
@@ -807,7 +818,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   rc = f.kind != kTensor ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl_lin, cluster)
                          : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl_lin);
   if (rc) return rc;
-  if (f.kind == kTensor) {
+  if (f.kind == kTensor || fold_mode == tfx::kFoldCombine) {
     // fold every block's slabs (one, when a unit covered all C chunks), rotate
     // back and store y: one warp per (row, block)
     CombineArgs ca = {};

@@ -74,6 +74,12 @@ struct Member {
   int cta_begin;            // first blockIdx.x of this member
 };
 
+// How the decode-rows kernel folds a block's C chunk sums: in the block's
+// cluster (distributed shared memory, two cluster barriers), through global
+// slabs summed by the last CTA to arrive on the block's counter, or through
+// global slabs summed by the combine kernel launched after it.
+constexpr int kFoldCluster = 0, kFoldCounter = 1, kFoldCombine = 2;
+
 struct LinearArgs {
   Member m[3];
   int count;
@@ -90,8 +96,8 @@ struct LinearArgs {
   int x_rows;       // warp-granular kernel: tile rows per x stage (the whole chunk, or H)
   int x_whole;      // warp-granular kernel: 1 if one x stage holds the whole chunk
   int fuse_rot;     // warp-granular kernel: 1 if each CTA rotates its chunk of x itself (few rows)
-  int fold_global;  // warp-granular kernel: 1 to fold a block's chunk sums through global slabs and
-                    // the block's counter (no cluster), 0 in the cluster's distributed shared memory
+  int fold_mode;    // warp-granular kernel: how a block's chunk sums are folded (kFoldCluster,
+                    // kFoldCounter, kFoldCombine)
   int early_arrive; // warp-granular kernel: 1 to arrive on the closing cluster barrier right after
                     // the fold's distributed loads (launches of many cluster waves)
   const void* x;    // the call's x (rows x K, act dtype), read when fuse_rot
@@ -1007,12 +1013,13 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
     while (clock64() - w0 < 2000000) {
     }
   }
-  if (a.fold_global) {
+  if (a.fold_mode != kFoldCluster) {
     // the launch has no clusters: this chunk's sums go to the block's slab
-    // [chunk][row][N] and the block's last CTA to arrive on its counter folds
-    // the C slabs in chunk order (the same balanced tree), rotates back, stores
-    // y and resets the counter (PR #1475's split-K form); no CTA waits for
-    // another, so launches of many cluster waves keep their SM slots busy
+    // [chunk][row][N]; with kFoldCounter the block's last CTA to arrive on its
+    // counter folds the C slabs in chunk order (the same balanced tree),
+    // rotates back, stores y and resets the counter (PR #1475's split-K form),
+    // with kFoldCombine the combine kernel does that for every (row, block) in
+    // parallel; either way no CTA waits for another
     if (!dead) {
       float* slab = M.partial + (long long)chunk * a.rp * M.N + nb * 128;
       const int g = lane >> 2, t = lane & 3;
@@ -1032,7 +1039,7 @@ __global__ void __launch_bounds__(32 * warp_cta_warps(NCOL)) linear_warp_kernel(
           }
         }
     }
-    if (arrive_last(M.counters + nb, M.C, &s_last)) {
+    if (a.fold_mode == kFoldCounter && arrive_last(M.counters + nb, M.C, &s_last)) {
       block_epilogue(M, a, 0, nb, a.rows, 0, warp, W, lane);
       if (threadIdx.x == 0) M.counters[nb] = 0;
     }

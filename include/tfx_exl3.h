@@ -179,16 +179,16 @@ int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
 
 /* Kernel family for the next calls. 0 = auto: 1..32 rows the warp-granular
  * decode-rows kernel (one cluster of C CTAs per 128-column block folds the C
- * chunk sums in distributed shared memory; launches of many blocks at few
- * rows, at most 4 rows and more than 128 blocks or at most 8 rows and more
- * than 512, fold through global slabs instead: the last CTA to arrive on the
- * block's counter sums them and resets it), every call above 32 rows the
+ * chunk sums in distributed shared memory; launches of more than 128 blocks,
+ * or more than 48 blocks at more than 8 rows, write the chunk sums to global
+ * slabs that a combine kernel folds instead), every call above 32 rows the
  * tensor-core kernel; 1 = for 1..64 rows the CTA decode-rows kernel whose split-K
  * partials are summed in-kernel by the last CTA to arrive on each block's
  * counter (the counter resets itself); 2 = the tensor-core kernel for every
  * row count; 3 = the warp-granular decode-rows kernel for every call of
- * 1..64 rows (fold chosen as in auto); 4 = as 3, with the global-slab fold
- * for every call of up to 8 rows. Rows a forced family does not serve go to
+ * 1..64 rows (fold chosen as in auto); 4 = as 3, for every call of up to 8
+ * rows with the chunk sums folded by the last CTA to arrive on the block's
+ * counter (which resets it). Rows a forced family does not serve go to
  * the tensor-core kernel. All give the same bytes. Initial value from
  * TFX_EXL3_VARIANT (auto|rows|mid|warp|warp_global). Returns the previous
  * value; a value outside 0..4 changes nothing. */

@@ -39,7 +39,7 @@ def _call_static(w, x, rows, y):
 
 @pytest.mark.parametrize("variant", [tfx.VARIANT_AUTO, tfx.VARIANT_ROWS, tfx.VARIANT_WARP_GLOBAL])
 @pytest.mark.parametrize("K,N,bits,rows,act", [(5120, 5120, 4, 16, tfx.F16), (5120, 1024, 3, 7, tfx.F16),
-                                               (1024, 2048, 4, 40, tfx.BF16)])
+                                               (1024, 2048, 4, 40, tfx.BF16), (1024, 20480, 3, 4, tfx.F16)])
 def test_static_entry_matches_linear_on_two_calls(K, N, bits, rows, act, variant):
     # VARIANT_ROWS sends 1..64 rows through the kernel whose split-K partials are
     # summed by the last CTA to arrive on each block's counter, VARIANT_WARP_GLOBAL
