@@ -27,7 +27,7 @@ ABI_SYMBOLS = ("tfx_exl3_linear", "tfx_exl3_group", "tfx_exl3_columns", "tfx_exl
                "tfx_exl3_debug_mark_events", "tfx_exl3_linear_static", "tfx_exl3_debug_error",
                "tfx_exl3_debug_launch_shape", "tfx_exl3_group_into", "tfx_exl3_debug_set_spin_limit",
                "tfx_exl3_debug_decode_rate", "tfx_exl3_chain", "tfx_exl3_encode", "tfx_exl3_encode_scratch_bytes",
-               "tfx_exl3_last_error")
+               "tfx_exl3_debug_launch_count", "tfx_exl3_last_error")
 
 
 class WeightStruct(C.Structure):
@@ -96,6 +96,8 @@ def lib() -> C.CDLL:
         for n in ABI_SYMBOLS[:-1]:
             getattr(L, n).restype = C.c_int
         L.tfx_exl3_debug_set_spin_limit.restype = C.c_int64
+        L.tfx_exl3_debug_launch_count.argtypes = []
+        L.tfx_exl3_debug_launch_count.restype = C.c_int64
         _lib = L
     return _lib
 
@@ -354,6 +356,11 @@ def decode_rate(bits: int, tiles_per_warp: int, sink=None, stream=None):
     _check(lib().tfx_exl3_debug_decode_rate(bits, tiles_per_warp, _ptr(sink) if sink is not None else None,
                                             C.byref(nf), C.byref(nw), _stream(stream) if sink is not None else None))
     return nw.value, nf.value
+
+
+def launch_count() -> int:
+    """Kernels the library has enqueued or captured since it was loaded."""
+    return lib().tfx_exl3_debug_launch_count()
 
 
 def set_pdl(mode) -> int:

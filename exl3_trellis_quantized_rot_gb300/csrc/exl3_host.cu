@@ -141,6 +141,7 @@ std::atomic<int> g_variant{env_variant()};
 thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 std::atomic<int> g_pdl{env_pdl()};
 std::atomic<long long> g_spin{tfx::kSpinClocks};
+std::atomic<long long> g_launches{0};  // kernels enqueued (or captured) through the library
 
 // ---------------------------------------------------------------- per-weight state
 
@@ -258,6 +259,7 @@ int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, v
   void* args[1] = {arg};
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   return 0;
 }
 
@@ -1011,6 +1013,8 @@ int tfx_exl3_set_variant(int variant) {
   if (variant < 0 || variant > 4) return g_variant.load();
   return g_variant.exchange(variant);
 }
+
+int64_t tfx_exl3_debug_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int tfx_exl3_set_pdl(int mode) {
   if (mode < 0 || mode > 2) return fail(TFX_EINVAL, "pdl mode %d (0, 1 or 2)", mode);

@@ -207,6 +207,11 @@ int tfx_exl3_set_variant(int variant);
 int tfx_exl3_debug_launch_shape(int K, int bits, int rows, int64_t blocks, int sm_count, int* family,
                                 int* chunks_per_unit);
 
+/* Kernels the library has enqueued on any stream (or recorded into a CUDA
+ * graph under capture) since it was loaded, counted on the host: the
+ * difference across one captured step is the step's launch count. */
+int64_t tfx_exl3_debug_launch_count(void);
+
 /* Programmatic dependent launch of the single and group calls (PR #1467,
  * "What this changes"): 0 off, 1 on every launch, 2 automatic (the default:
  * on the rotation launch and the decode-rows linear launch of a call that has

@@ -290,6 +290,21 @@ def test_output_window_validation_before_any_launch(L, drv):
     assert rc == tfx.ENOTRESERVED
 
 
+def test_launch_count_moves_only_with_launches(L, drv):
+    # the count the benchmark reads around a captured step: calls rejected on
+    # the host and zero-row calls enqueue nothing
+    w = fake_weight(256, 256, 4)
+    tfx.reserve(w, 4, 0)
+    n0 = tfx.launch_count()
+    assert n0 >= 0
+    arr = (C.POINTER(tfx.WeightStruct) * 1)(C.pointer(w.s))
+    ys = (C.c_void_p * 1)(FAKE + (4 << 30))
+    assert L.tfx_exl3_group(arr, 1, FAKE + (3 << 30), 0, ys, None) == 0
+    assert L.tfx_exl3_group(arr, 1, FAKE + (3 << 30), 9, ys, None) == tfx.ENOTRESERVED
+    assert L.tfx_exl3_group(arr, 1, FAKE + 3, 1, ys, None) == tfx.EALIGN
+    assert tfx.launch_count() == n0
+
+
 def test_spin_limit_and_decode_rate_query(L):
     old = tfx.set_spin_limit(7)
     assert old == 2_000_000_000
