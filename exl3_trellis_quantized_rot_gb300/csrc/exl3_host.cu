@@ -301,10 +301,10 @@ constexpr long long kEarlyArriveClusters = 128;
 //     147 / 148 / 151; the 6-bit LM head (1940 blocks): 433 / 435 / 438,
 //     358 / 364 / 374, 352 / 361 / 371.
 // The last-arriver counter form (PR #1475) is the forced variant 4 (up to
-// kFoldGlobalRows rows).
-constexpr int kFoldGlobalRows = 8;
+// kFoldCounterRows rows).
+constexpr int kFoldCounterRows = 8;
 int fold_mode_for(int rows, long long blocks) {
-  if (g_variant.load(std::memory_order_relaxed) == 4 && rows <= kFoldGlobalRows) return tfx::kFoldCounter;
+  if (g_variant.load(std::memory_order_relaxed) == 4 && rows <= kFoldCounterRows) return tfx::kFoldCounter;
   if (blocks > 128 || (blocks > 48 && rows > 8)) return tfx::kFoldCombine;
   return tfx::kFoldCluster;
 }
@@ -693,7 +693,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   long long all_blocks = 0;
   for (int i = 0; i < count; i++) all_blocks += ws[i]->N / 128;
   const int fold_mode = f.kind == kRowsWarp ? fold_mode_for(rows, all_blocks) : tfx::kFoldCluster;
-  const bool fold_global = fold_mode != tfx::kFoldCluster;
+  const bool fold_slabs = fold_mode != tfx::kFoldCluster;  // no clusters: chunk sums in global slabs
   if (f.kind == kTensor) {
     long long blocks = 0;
     for (int i = 0; i < count; i++) blocks += ws[i]->N / 128;
@@ -721,7 +721,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
       // cluster that folds the chunk sums in distributed shared memory
       m.G = 1;
       m.TC = f.ncol;
-      m.P = fold_global ? m.C : 1;  // slabs of a block: one per chunk with the global fold
+      m.P = fold_slabs ? m.C : 1;  // slabs of a block: one per chunk when folded through slabs
       m.arrivals = fold_mode == tfx::kFoldCounter ? m.C : 0;
       ctas += (long long)m.NB * m.C;
     } else if (f.kind == kRowsCta) {
@@ -816,7 +816,7 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   cudaEvent_t eb = g_ev_before, ea = g_ev_after;
   g_ev_before = g_ev_after = nullptr;
   if (eb && record_event(eb, s) != cudaSuccess) return fail(TFX_ECUDA, "cudaEventRecord");
-  const int cluster = f.kind == kRowsWarp && !fold_global ? chunks_of(K) : 1;
+  const int cluster = f.kind == kRowsWarp && !fold_slabs ? chunks_of(K) : 1;
   rc = f.kind != kTensor ? launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &la, pdl_lin, cluster)
                          : launch(f.fn, dim3((unsigned)ctas), dim3(f.wpc * 32), smem, s, &ta, pdl_lin);
   if (rc) return rc;
