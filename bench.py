@@ -683,8 +683,9 @@ def run_gpu(args):
             "detail": detail,
             "roofline": {"bound": "alu", "achieved": round(dec_achieved, 1), "peak": round(dec_peak, 1),
                          "unit": "G decoded weights/s", "frac": round(dec_achieved / dec_peak, 4), "traffic": traffic,
-                         "kernel": "linear_warp_kernel<4,2,2> (decode rows, cluster split-K), group + single call",
-                         "timing": "whole timed step (rotation launches included) per step",
+                         "kernel": "linear_warp_kernel<4,2,2> (decode rows; q/k/v group folded through global slabs "
+                                   "and the combine kernel, 5120x5120 in its clusters), group + single call",
+                         "timing": "whole timed step (rotation and combine launches included) per step",
                          "peak_source": f"measured in this run: tfx_exl3_debug_decode_rate probe ({probe_w / 1e9:.2f} "
                                         f"G weights per launch, best of 5 launches, {min(probe_ms) * 1e3:.1f} us)",
                          "hbm": {"achieved": round(hbm_achieved, 1), "peak": peak, "unit": "GB/s",
