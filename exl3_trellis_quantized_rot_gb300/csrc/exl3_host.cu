@@ -284,6 +284,8 @@ constexpr long long kFuseRotWeights = 64LL << 20;
 // Decode-rows launches of more clusters than this arrive early on the closing
 // cluster barrier (LinearArgs::early_arrive).
 constexpr long long kEarlyArriveClusters = 128;
+// auto sends calls of up to this many rows to the decode-rows kernel.
+constexpr int kAutoRowsMax = 16;
 // How the decode-rows kernel folds a block's chunk sums (LinearArgs::fold_mode).
 // In the block's cluster every CTA waits at the cluster barrier for its
 // slowest chunk while holding its SM slot; with many blocks that wait is what
@@ -309,13 +311,15 @@ int fold_mode_for(int rows, long long blocks) {
   return tfx::kFoldCluster;
 }
 
-// Kernel choice. auto: up to 32 rows the warp-granular decode-rows kernel,
+// Kernel choice. auto: up to 16 rows the warp-granular decode-rows kernel,
 // above that the persistent tensor-core kernel (measured on GB300, 4-bit,
-// K = 5120, graph-replayed calls: at 40..64 rows 5120 x 5120 34-35 us against
-// 43-47 us, the q/k/v group 39-40 us against 69-75 us, gate+up 128-131 us
-// against 251-275 us; at 24..32 rows the decode-rows kernel is faster or even).
-// The other variants force a family where it serves the row count (all give
-// the same bytes).
+// K = 5120, graph-replayed calls, decode-rows against tensor core: 5120 x 5120
+// at 12 / 16 / 20 / 32 rows 15.4 / 16.1 / 25.2 / 25.8 us against 25.1 / 25.1 /
+// 25.6 / 25.9; the q/k/v group 21.8 / 22.3 / 32.9 / 34.5 against 30.2 / 30.4 /
+// 31.0 / 31.3; gate+up 58.4 / 58.6 / 111.6 / 118.3 against 88.8 / 89.5 / 90.2 /
+// 91.2: above 16 rows the decode-rows kernel's row tile doubles its MMAs per
+// decoded tile). The other variants force a family where it serves the row
+// count (all give the same bytes).
 Family pick(int bits, int rows) {
   const tfx::KernelSet& ks = kernels(bits);
   const int i = rows <= tfx::kRowsMaxRows ? row_tile(rows) : 0;
@@ -329,7 +333,7 @@ Family pick(int bits, int rows) {
     case 3:
     case 4: return rows <= tfx::kRowsMaxRows ? warpk : tc;
     default:
-      if (rows <= 32) return warpk;
+      if (rows <= kAutoRowsMax) return warpk;
       return tc;
   }
 }

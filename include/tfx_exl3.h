@@ -177,11 +177,11 @@ int tfx_exl3_plan(const tfx_exl3_weight* w, int* chunks, int* tiles_per_chunk);
 /* Allocations and counter memsets made for this weight since its creation. */
 int tfx_exl3_stats(const tfx_exl3_weight* w, int64_t* allocs, int64_t* memsets);
 
-/* Kernel family for the next calls. 0 = auto: 1..32 rows the warp-granular
+/* Kernel family for the next calls. 0 = auto: 1..16 rows the warp-granular
  * decode-rows kernel (one cluster of C CTAs per 128-column block folds the C
  * chunk sums in distributed shared memory; launches of more than 128 blocks,
  * or more than 48 blocks at more than 8 rows, write the chunk sums to global
- * slabs that a combine kernel folds instead), every call above 32 rows the
+ * slabs that a combine kernel folds instead), every call above 16 rows the
  * tensor-core kernel; 1 = for 1..64 rows the CTA decode-rows kernel whose split-K
  * partials are summed in-kernel by the last CTA to arrive on each block's
  * counter (the counter resets itself); 2 = the tensor-core kernel for every

@@ -215,7 +215,7 @@ def test_variant_and_pdl_switches(L):
 
 
 def test_kernel_choice_and_tensor_core_unit_size(L):
-    """The launch-shape rules (host only): auto sends 1..32 rows to the
+    """The launch-shape rules (host only): auto sends 1..16 rows to the
     warp-granular decode-rows kernel and every longer call to the tensor-core
     kernel; the tensor-core unit size G (chunks of K per unit) is the measured
     best for the 27B shapes on 152 SMs and always fits TMEM; forced variants
@@ -224,9 +224,9 @@ def test_kernel_choice_and_tensor_core_unit_size(L):
     shape = tfx.debug_launch_shape
     old = tfx.set_variant(tfx.VARIANT_AUTO)
     try:
-        for rows in (1, 7, 8, 9, 16, 17, 31, 32):
+        for rows in (1, 7, 8, 9, 16):
             assert shape(5120, 4, rows, 40, 152) == (tfx.FAMILY_ROWS_WARP, 0), rows
-        for rows in (33, 48, 64, 65, 100, 128, 129, 4096):
+        for rows in (17, 31, 32, 33, 48, 64, 65, 100, 128, 129, 4096):
             assert shape(5120, 4, rows, 40, 152)[0] == tfx.FAMILY_TENSOR, rows
         # G on 152 SMs, K = 5120 (16 chunks): 5120 x 5120 (40 blocks), the q/k/v group (64 blocks), gate+up (272)
         want = {(40, 64): 2, (40, 128): 2, (64, 64): 8, (64, 128): 8, (272, 64): 16, (272, 128): 16}
