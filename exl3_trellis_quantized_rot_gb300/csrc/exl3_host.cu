@@ -124,10 +124,9 @@ int env_variant() {
 }
 // Programmatic dependent launch: 0 off, 1 on every kernel, 2 (the default)
 // automatic: on the rotation launch and on the decode-rows linear launch that
-// follows it, on the combine launch after a decode-rows launch that folds
+// follows it, and on the combine launch after a decode-rows launch that folds
 // through slabs (measured on GB300: the q/k/v group at 16 rows 22.6 -> 21.8
-// us), and on every launch of a tensor-core call (5120 x 5120 at 128 rows
-// 30.7 -> 30.3 us); not on fused-rotation decode-rows launches. Measured on GB300 inside CUDA graphs (calls back
+// us), nowhere else. Measured on GB300 inside CUDA graphs (calls back
 // to back, K = 5120, 4-bit): with it on every kernel a 1-row 5120 x 5120 call
 // (one fused kernel, no rotation launch) takes 14.3 us against 13.0 without;
 // on the rotation and decode-rows launches of 7- and 16-row calls it saves
@@ -811,9 +810,9 @@ int launch_layer(tfx_exl3_weight* const ws[], int count, const void* x, int rows
   // programmatic dependent launch per kernel (see env_pdl): in the automatic
   // mode only a decode-rows call with its own rotation launch takes it, on
   // both of its launches
-  const bool pdl_auto = pdl == 2 && ((f.kind == kRowsWarp && !la.fuse_rot) || f.kind == kTensor);
+  const bool pdl_auto = pdl == 2 && f.kind == kRowsWarp && !la.fuse_rot;
   const bool pdl_rot = pdl == 1 || pdl_auto, pdl_lin = pdl == 1 || pdl_auto;
-  const bool pdl_comb = pdl == 1 || (pdl == 2 && (fold_mode == tfx::kFoldCombine || f.kind == kTensor));
+  const bool pdl_comb = pdl == 1 || (pdl == 2 && fold_mode == tfx::kFoldCombine);
   // everything that can fail on the host is done: enqueue the rotation, then the linear kernel
   if (!la.fuse_rot) {
     rc = launch(reinterpret_cast<const void*>(&rot_kernel), dim3((unsigned)((items + 7) / 8)), dim3(256), 0, s, &ra,

@@ -215,9 +215,9 @@ int64_t tfx_exl3_debug_launch_count(void);
 /* Programmatic dependent launch of the single and group calls (PR #1467,
  * "What this changes"): 0 off, 1 on every launch, 2 automatic (the default:
  * on the rotation launch and the decode-rows linear launch of a call that has
- * both, on the combine launch that folds a decode-rows launch's slabs, and on
- * every launch of a tensor-core call; off for fused-rotation decode-rows
- * launches, the choice that measured fastest inside CUDA graphs). Initial value from TFX_EXL3_PDL
+ * both, and on the combine launch that folds a decode-rows launch's slabs;
+ * off for fused-rotation and tensor-core launches and the tensor-core
+ * combine, the choice that measured fastest inside CUDA graphs). Initial value from TFX_EXL3_PDL
  * ("0" or "1"; unset or anything else: 2). Returns the previous mode, or
  * TFX_EINVAL for a mode outside 0..2 (nothing changed). The static-scratch
  * entry point never uses it. */
