@@ -44,11 +44,20 @@ __global__ void __launch_bounds__(256) rot_kernel(const __grid_constant__ RotArg
   if (item >= (long long)a.rows_pad * nblk) return;
   const int r = (int)(item / nblk);
   const int b = (int)(item % nblk);
+  // every member's suh is requested together with x: inside the member loop
+  // each load would wait for the previous member's stores (the compiler cannot
+  // move a load across stores that may alias it)
+  uint2 su[3];
+#pragma unroll
+  for (int m = 0; m < 3; m++)
+    if (m < a.count) su[m] = rot_suh(a, m, b, lane);
   float xv[4];
   rot_load(a, r, b, lane, xv);
-  for (int m = 0; m < a.count; m++) {
+#pragma unroll
+  for (int m = 0; m < 3; m++) {
+    if (m >= a.count) break;
     __half2 h[2];
-    rot_member(a, m, b, lane, xv, h);
+    rot_member_su(su[m], lane, xv, h);
     if (a.layout == 0) {
       rot_store_frag(a, m, r, b, lane, h);
     } else {

@@ -297,15 +297,21 @@ __device__ __forceinline__ void rot_load(const RotArgs& a, int r, int b, int lan
 }
 
 // fp16(Hn(suh_m o x)) of one 128-block, the lane's 4 values as two half2.
-__device__ __forceinline__ void rot_member(const RotArgs& a, int m, int b, int lane, const float (&xv)[4],
-                                           __half2 (&h)[2]) {
-  uint2 su = *reinterpret_cast<const uint2*>(a.suh[m] + 128LL * b + 4 * lane);
+// suh of member m for the lane's 4 elements of 128-block b.
+__device__ __forceinline__ uint2 rot_suh(const RotArgs& a, int m, int b, int lane) {
+  return *reinterpret_cast<const uint2*>(a.suh[m] + 128LL * b + 4 * lane);
+}
+__device__ __forceinline__ void rot_member_su(uint2 su, int lane, const float (&xv)[4], __half2 (&h)[2]) {
   __half2 s0 = *reinterpret_cast<__half2*>(&su.x), s1 = *reinterpret_cast<__half2*>(&su.y);
   float v[4] = {xv[0] * __low2float(s0), xv[1] * __high2float(s0), xv[2] * __low2float(s1), xv[3] * __high2float(s1)};
   fwht128(v, lane);
 #pragma unroll
   for (int mm = 0; mm < 2; mm++)
     h[mm] = __halves2half2(__float2half_rn(v[2 * mm] * kInvSqrt128), __float2half_rn(v[2 * mm + 1] * kInvSqrt128));
+}
+__device__ __forceinline__ void rot_member(const RotArgs& a, int m, int b, int lane, const float (&xv)[4],
+                                           __half2 (&h)[2]) {
+  rot_member_su(rot_suh(a, m, b, lane), lane, xv, h);
 }
 
 // Store in B-fragment order: element k = 128b + 4*lane + e sits in tile 8b + lane/4
