@@ -41,6 +41,8 @@ def packed_bytes(Kk, N, bits):
 
 
 STEP_WEIGHT_BYTES = sum(packed_bytes(K, n, BITS) for n in QKV) + packed_bytes(K, O_N, BITS)
+STEP_WORKLOAD = ("decode rows at 27B shapes: q/k/v group (6144+1024+1024) + single 5120x5120, K=5120, "
+                 "4-bit, 16 rows FP16")
 
 
 def load_peaks():
@@ -143,34 +145,49 @@ def whole_job(ms_local: float, steps: int, ws: int, device) -> tuple[float, floa
 
 # ---------------------------------------------------------------------------- CPU oracle leg
 
-def _oracle_inputs(n):
+def _step_blocks():
+    """The headline step's 128-column blocks in order: (member, N, block) for
+    the q/k/v group's three weights and the single 5120 x 5120 weight."""
+    return [(m, n, b) for m, n in enumerate(QKV + (O_N,)) for b in range(n // 128)]
+
+
+def _step_inputs():
+    """The step's four weights and x as rank 0 of the GPU arm draws them, in
+    the oracle's FP64 form."""
     import numpy as np
 
     import oracle
     import synth
-    codes = synth.codes(0, K, O_N, BITS)
-    suh = synth.suh(0, K).astype(np.float64)
-    svh = synth.svh(0, O_N).astype(np.float64)
-    x = synth.as_f64(synth.activations(0, ROWS, K, "f16"), "f16")
+    seed = 1000
+    members = []
+    for m, n in enumerate(QKV + (O_N,)):
+        members.append((synth.codes(seed, K, n, BITS, m), synth.suh(seed, K, m).astype(np.float64),
+                        synth.svh(seed, n, m).astype(np.float64)))
+    x = synth.as_f64(synth.activations(seed, ROWS, K, "f16"), "f16")
     oracle.lib()
-    return codes, suh, svh, x
+    return members, x
+
+
+def _oracle_block(inp, i):
+    """The oracle as it stands on block i of the step (one call, its rotation included)."""
+    import oracle
+    members, x = inp
+    m, n, b = _step_blocks()[i]
+    codes, suh, svh = members[m]
+    oracle.linear(codes, K, 128, BITS, suh, svh[128 * b:128 * b + 128], x, tile_row_stride=(n // 16) * 8 * BITS,
+                  col_from=128 * b)
 
 
 _W = {}
 
 
 def _oracle_worker_init():
-    _W["inp"] = _oracle_inputs(O_N)
+    _W["inp"] = _step_inputs()
 
 
-def _oracle_worker_block(blk):
-    """The oracle on 128-column block blk of the 5120 x 5120 layer (one worker)."""
-    import oracle
-    codes, suh, svh, x = _W["inp"]
-    c0 = 128 * blk
-    oracle.linear(codes, K, 128, BITS, suh, svh[c0:c0 + 128], x, tile_row_stride=(O_N // 16) * 8 * BITS,
-                  col_from=c0)
-    return blk
+def _oracle_worker_block(i):
+    _oracle_block(_W["inp"], i)
+    return i
 
 
 def host_cores() -> int:
@@ -192,26 +209,25 @@ def cpu_model() -> str:
 
 
 def oracle_sample(seconds_budget: float = 12.0):
-    """Time the CPU oracle as it stands on two bounded samples of the workload:
-    one core on columns [0, 512) of the 5120 x 5120 layer at 16 rows, and every
-    host core on the whole 5120 x 5120 layer at 16 rows (its 40 blocks of 128
-    columns spread over a pool of spawned worker processes, each running the
+    """Time the CPU oracle as it stands on two bounded samples of the headline
+    step: one core walking the step's 128-column blocks in order (one oracle
+    call per block), and every host core on the whole step (its 104 blocks
+    spread over a pool of spawned worker processes, each running the
     single-threaded oracle on one block at a time)."""
     import multiprocessing as mp
 
-    import oracle
-    n = 512
-    codes, suh, svh, x = _oracle_inputs(n)
+    inp = _step_inputs()
+    nblk = len(_step_blocks())
     times = []
     t_end = time.perf_counter() + seconds_budget / 2
     while True:
         t0 = time.perf_counter()
-        oracle.linear(codes, K, n, BITS, suh, svh[:n], x, tile_row_stride=(O_N // 16) * 8 * BITS)
+        _oracle_block(inp, len(times) % nblk)
         times.append(time.perf_counter() - t0)
-        if time.perf_counter() > t_end or len(times) >= 50:
+        if (time.perf_counter() > t_end and len(times) >= 8) or len(times) >= nblk:
             break
     sec1 = statistics.median(times)
-    gbs1 = packed_bytes(K, n, BITS) / sec1 / 1e9
+    gbs1 = packed_bytes(K, 128, BITS) / sec1 / 1e9
     cores = host_cores()
     ctx = mp.get_context("spawn")
     with ctx.Pool(cores, initializer=_oracle_worker_init) as pool:
@@ -220,39 +236,47 @@ def oracle_sample(seconds_budget: float = 12.0):
         t_end = time.perf_counter() + seconds_budget / 2
         while True:
             t0 = time.perf_counter()
-            pool.map(_oracle_worker_block, range(O_N // 128), chunksize=1)
+            pool.map(_oracle_worker_block, range(nblk), chunksize=1)
             ptimes.append(time.perf_counter() - t0)
             if time.perf_counter() > t_end or len(ptimes) >= 20:
                 break
     secp = statistics.median(ptimes)
-    gbsp = packed_bytes(K, O_N, BITS) / secp / 1e9
+    gbsp = STEP_WEIGHT_BYTES / secp / 1e9
     return {"value": round(gbsp, 5), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "cpu": cpu_model(),
-            "sample": f"the whole 5120x5120 4-bit layer at {ROWS} rows, its 40 column blocks spread over "
+            "sample": f"the whole step (q/k/v group + 5120x5120, {ROWS} rows), its {nblk} column blocks spread over "
                       f"{cores} spawned processes each running the FP64 single-thread C oracle; median of "
-                      f"{len(ptimes)} layers ({secp * 1e3:.1f} ms per layer)",
+                      f"{len(ptimes)} steps ({secp * 1e3:.1f} ms per step)",
             "single_core": {"value": round(gbs1, 5), "unit": "GB/s", "cores": 1,
-                            "sample": f"5120x{n} columns of the same layer, {ROWS} rows, one core; median of "
-                                      f"{len(times)} calls ({sec1 * 1e3:.1f} ms/call)"}}
+                            "sample": f"the step's first {len(times)} 128-column blocks, {ROWS} rows, one core, "
+                                      f"one oracle call each; median {sec1 * 1e3:.1f} ms per block"}}
+
+
+def step_config(ws: int) -> dict:
+    """The workload keys both arms report (the GPU arm adds how it times)."""
+    return {"workload": STEP_WORKLOAD, "K": K, "bits": BITS, "rows": ROWS, "weights_per_step_bytes": STEP_WEIGHT_BYTES,
+            "parallelism": f"replicas x{ws}"}
 
 
 def run_reference(args):
+    """The oracle as it stands, timed on the host's cores, on the headline
+    step's workload: the same weights and x as rank 0 of the GPU arm, walked
+    one 128-column block per oracle call through the step's 104 blocks (q, k,
+    v, then the 5120 x 5120 weight; every block has the same K, so each is a
+    fair sample of the step), as many blocks per step as keep the whole run at
+    about 2000 calls."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    import numpy as np
-
-    import oracle
-    import synth
-    n = 512
-    codes = synth.codes(0, K, O_N, BITS)
-    suh = synth.suh(0, K).astype(np.float64)
-    svh = synth.svh(0, O_N).astype(np.float64)
-    x = synth.as_f64(synth.activations(0, ROWS, K, "f16"), "f16")
-    oracle.lib()
+    inp = _step_inputs()
+    blocks = _step_blocks()
+    per_step = max(1, min(len(blocks), 2000 // max(1, args.steps + args.warmup)))
+    pos = [0]
 
     def step():
-        oracle.linear(codes, K, n, BITS, suh, svh[:n], x, tile_row_stride=(O_N // 16) * 8 * BITS)
+        for _ in range(per_step):
+            _oracle_block(inp, pos[0] % len(blocks))
+            pos[0] += 1
 
     for _ in range(args.warmup):
         step()
@@ -260,14 +284,17 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     sec = (time.perf_counter() - t0) / args.steps
-    gbs = packed_bytes(K, n, BITS) / sec / 1e9
-    sample = (f"5120x{n} columns of the 5120x5120 4-bit layer, {ROWS} rows, per step; FP64 single-thread C oracle")
+    gbs = per_step * packed_bytes(K, 128, BITS) / sec / 1e9
+    sample = (f"{per_step} of the step's {len(blocks)} 128-column blocks per step (q/k/v group then the 5120x5120 "
+              f"weight, in turn), {ROWS} rows; FP64 single-thread C oracle, one call per block")
+    cfg = step_config(ws)
+    cfg["l2"] = "n/a (host)"
+    cfg["timing"] = "host wall clock over K steps after W warm-up steps"
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode rows at 27B shapes (sampled columns)", "K": K, "N": O_N, "bits": BITS,
-                       "rows": ROWS},
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+                             "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -672,13 +699,10 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(sec_per_step * 1e3, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": {"workload": "decode rows at 27B shapes: q/k/v group (6144+1024+1024) + single 5120x5120, "
-                                   "K=5120, 4-bit, 16 rows FP16",
-                       "K": K, "bits": BITS, "rows": ROWS, "weights_per_step_bytes": STEP_WEIGHT_BYTES,
+            "config": {**step_config(ws),
                        "l2": f"weights cycled through {copies} distinct copies "
                              f"({copies * STEP_WEIGHT_BYTES / 1e6:.0f} MB > 4x L2)",
-                       "timing": "K steps replayed from one CUDA graph, CUDA events on the launching stream",
-                       "parallelism": f"replicas x{ws}"},
+                       "timing": "K steps replayed from one CUDA graph, CUDA events on the launching stream"},
             "us_per_step": round(sec_per_step * 1e6, 3),
             "detail": detail,
             "roofline": {"bound": "alu", "achieved": round(dec_achieved, 1), "peak": round(dec_peak, 1),

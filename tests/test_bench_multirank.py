@@ -7,6 +7,7 @@ milliseconds and the whole-job throughput (all ranks' bytes over the slowest
 rank's time). These run here with world size 2 and no GPU; the reference arm's
 rule that ranks other than 0 exit without work is checked too.
 """
+import json
 import os
 import socket
 
@@ -67,3 +68,24 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 
     assert bench.run_reference(Args()) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_reports_the_gpu_arms_workload(monkeypatch, capsys):
+    # rank 0 alone, on two of the step's blocks so that the test stays short
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    blocks = bench._step_blocks()
+    assert len(blocks) == sum(bench.QKV + (bench.O_N,)) // 128
+    assert blocks[0] == (0, bench.QKV[0], 0) and blocks[-1] == (3, bench.O_N, bench.O_N // 128 - 1)
+    monkeypatch.setattr(bench, "_step_blocks", lambda: blocks[47:49])  # last q block, first k block
+
+    class Args:
+        steps, warmup = 2, 3
+
+    assert bench.run_reference(Args()) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
+    assert {k: line["config"][k] for k in bench.step_config(1)} == bench.step_config(1)
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["value"] == line["value"] == line["e2e"]["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
