@@ -243,6 +243,38 @@ def test_gate_up_group_mid_rows():
                          what=f"gate/up rows={rows}")
 
 
+@pytest.mark.parametrize("rows", [40, 128, 200])
+def test_qkv_group_at_tensor_core_rows(rows):
+    """q/k/v (N = 6144, 1024, 1024) as one group at tensor-core row counts: the
+    persistent grid walks units of three members of unequal N (and 200 rows
+    take two passes); each member's bytes equal its own call, and its first
+    and last blocks match the oracle."""
+    ws = [make(2, 5120, N, 4, member=m, max_rows=200) for m, N in enumerate((6144, 1024, 1024))]
+    x64, x = x_of(41, rows, 5120)
+    ys = tfx.group([w for _, w in ws], x)
+    for (hw, w), y in zip(ws, ys):
+        assert same_bytes(y, tfx.linear(w, x)), (hw.N, rows)
+        for blk in (0, hw.N // 128 - 1):
+            assert_close(to_f64(y[:, 128 * blk:128 * blk + 128]), oracle_y(hw, x64, 128 * blk, 128),
+                         what=f"q/k/v group N={hw.N} rows={rows} blk={blk}")
+        assert tfx.device_error(w) == 0
+
+
+@pytest.mark.parametrize("rows", [40, 128, 200])
+def test_column_view_at_tensor_core_rows(rows):
+    """A view of blocks [4, 12) of a 1024 x 2048 6-bit weight at tensor-core row
+    counts gives the bytes of the same columns of the full call (the view keeps
+    the parent's strides and plan), and its first block matches the oracle."""
+    hw, w = make(43, 1024, 2048, 6, act=tfx.BF16, max_rows=200)
+    v = tfx.columns(w, 512, 1024)
+    tfx.reserve(v, 200)
+    x64, x = x_of(43, rows, 1024, tfx.BF16)
+    full = tfx.linear(w, x)
+    yv = tfx.linear(v, x)
+    assert same_bytes(yv, full[:, 512:1536]), rows
+    assert_close(to_f64(yv[:, :128]), oracle_y(hw, x64, 512, 128), tfx.BF16, what=f"view rows={rows}")
+
+
 def test_prefill_4096_rows():
     hw, w = make(9, 5120, 17408, 4, act=tfx.BF16, max_rows=4096)
     x64, x = x_of(9, 4096, 5120, tfx.BF16)
